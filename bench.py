@@ -1,0 +1,490 @@
+"""Benchmark: paged varlen GQA attention on GB300.
+
+Default workload: long-context sliding-window decode (batch 8, kv_len 6700, window
+4096, 32 q / 8 kv heads, head_dim 128, per-head sinks, bf16 KV), the shape the
+pages quote decode tokens/s on.  One step is one ``ua_unified_attention`` call (the
+split-KV partition kernel plus the merge kernel).  The cache holds several replicas
+of the working set on disjoint physical blocks and step i reads replica i mod R, so
+consecutive steps never hit L2 (R x algorithmic bytes > 3 x L2).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU fp64 oracle on
+the host cores on the same workload instead (a deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# --------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "varlen_gqa_attention_paged_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d[kernel_key]
+        if rec.get("source_hash") != kernel_source_hash():
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU works (start before, stop after)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = {}
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu=timestamp,{self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "25"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        t0, t1 = self.marks.get("timed_start"), self.marks.get("timed_end")
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(ts=ts, sm=float(parts[2]), sm_max=float(parts[3]),
+                                 active=parts[5], hw=parts[6], hwt=parts[7], swt=parts[8],
+                                 swpc=parts[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        window = "timed"
+        sel = [r for r in rows if t0 is not None and t0 - 0.03 <= r["ts"] <= t1 + 0.03]
+        if not sel:
+            sel, window = rows, "whole run"
+        reasons = set()
+        for r in sel:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swpc", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in sel),
+                "sm_max_mhz": max(r["sm_max"] for r in sel), "reasons": sorted(reasons),
+                "samples": len(sel), "window": window}
+
+
+# --------------------------------------------------------------------------- our arm
+
+class Call:
+    """Pre-marshalled arguments of ua_unified_attention for one input set on the GPU."""
+
+    def __init__(self, inp, dev, backend="auto", replica=0):
+        import varlen_gqa_attention_paged_gb300 as ua
+        from varlen_gqa_attention_paged_gb300 import _lib
+        self.ua, self.lib = ua, _lib.load()
+        self.inp = inp
+        self.d = {n: (None if getattr(inp, n) is None else getattr(inp, n).to(dev).contiguous())
+                  for n in ("q", "k_cache", "v_cache", "cu_seqlens_q", "seq_lens_k",
+                            "block_table", "alibi_slopes", "qq_bias", "sinks")}
+        bt = self.d["block_table"]
+        self.tables = [bt] if bt.dim() == 2 else [bt[r].contiguous() for r in range(bt.shape[0])]
+        self.kv_scale = None
+        if inp.spec.kv_dtype == torch.float8_e4m3fn:
+            self.kv_scale = torch.tensor([inp.k_scale, inp.v_scale], dtype=torch.float32,
+                                         device=dev)
+        self.out = torch.empty_like(self.d["q"])
+        self.backend = ua.BACKENDS[backend]
+        self.plan = ua.plan(num_seqs=inp.num_seqs, total_q=inp.total_q,
+                            max_seqlen_q=inp.max_seqlen_q, max_seqlen_k=inp.max_seqlen_k,
+                            block_size=inp.spec.block_size, num_q_heads=inp.spec.num_q_heads,
+                            num_kv_heads=inp.spec.num_kv_heads, head_dim=inp.spec.head_dim,
+                            window_left=inp.window_left,
+                            kv_dtype=ua._DTYPES[inp.spec.kv_dtype],
+                            q_dtype=ua._DTYPES[inp.spec.q_dtype], backend=backend,
+                            max_blocks_per_seq=self.tables[0].shape[-1],
+                            num_blocks=self.d["k_cache"].shape[0])
+        self.shape = ua._shape(self.d["q"], self.d["k_cache"], self.tables[0],
+                               self.d["cu_seqlens_q"], inp.max_seqlen_q, inp.max_seqlen_k,
+                               self.d["qq_bias"], ua._DTYPES[self.out.dtype], 0, None, None)
+        p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+        spec = inp.spec
+        self.head = [p(self.d["q"]), p(self.d["k_cache"]), p(self.d["v_cache"]), p(self.out),
+                     p(self.d["cu_seqlens_q"]), p(self.d["seq_lens_k"])]
+        self.table_ptrs = [p(t) for t in self.tables]
+        self.tail = [spec.block_size, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                     float(inp.scale), float(inp.softcap), int(inp.window_left),
+                     p(self.d["alibi_slopes"]), p(self.d["qq_bias"]), p(self.d["sinks"]),
+                     ua._DTYPES[spec.kv_dtype], p(self.kv_scale), self.backend]
+        self.launches_per_call = 2 if self.plan["path"] == ua.UA_PATH_SPLIT else 1
+
+    def __call__(self, stream, replica=0, events=None):
+        if events is not None:
+            self.shape.events = ctypes.cast(events, ctypes.c_void_p)
+        else:
+            self.shape.events = None
+        rc = self.lib.ua_unified_attention(*self.head, self.table_ptrs[replica % len(self.tables)],
+                                           *self.tail, ctypes.c_void_p(stream.cuda_stream),
+                                           ctypes.byref(self.shape))
+        if rc != 0:
+            raise self.ua.UaError(rc, "ua_unified_attention")
+
+
+def event_triplets(n):
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    arrs = [(ctypes.c_void_p * 3)(*[e.cuda_event for e in trip]) for trip in evs]
+    return evs, arrs
+
+
+def n_replicas(spec):
+    """Cache replicas so that R x per-step KV bytes exceed 3 x L2 (bounded)."""
+    esz = torch.empty((), dtype=spec.kv_dtype).element_size()
+    keys = 0
+    for a, kv in spec.seqs:
+        lo = 0 if not spec.window else max(0, kv - a - (spec.window - 1))
+        keys += kv - lo
+    per_step = keys * spec.num_kv_heads * spec.head_dim * esz * 2
+    return int(min(64, max(1, math.ceil(3 * L2_BYTES / max(per_step, 1)))))
+
+
+def measure_workload(spec, dev, stream, steps, warmup, backend="auto"):
+    """Device time per call (library events around each kernel), median over calls."""
+    reps = n_replicas(spec)
+    inp = W.make(spec, replicas=reps)
+    call = Call(inp, dev, backend=backend)
+    evs, arrs = event_triplets(steps)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            call(stream, replica=i)
+        torch.cuda.synchronize()
+        for i in range(steps):
+            call(stream, replica=i, events=arrs[i])
+        torch.cuda.synchronize()
+    attn = [evs[i][0].elapsed_time(evs[i][1]) for i in range(steps)]
+    total = [evs[i][0].elapsed_time(evs[i][2]) for i in range(steps)]
+    return inp, call, reps, attn, total
+
+
+def workload_record(inp, call, reps, attn_ms, total_ms, hbm_peak, tc_peak):
+    spec = inp.spec
+    med = statistics.median(total_ms)
+    kbytes = W.kv_bytes_read(inp)
+    flops = W.attention_flops(inp)
+    rec = {"path": "split" if call.plan["path"] == 2 else "2d", "n_part": call.plan["n_part"],
+           "kernel_block_m": call.plan["block_m"], "us_per_call": round(med * 1e3, 2),
+           "attn_kernel_us": round(statistics.median(attn_ms) * 1e3, 2),
+           "tokens_per_s": round(inp.total_q / (med * 1e-3), 1),
+           "kv_gbs": round(kbytes / (med * 1e-3) / 1e9, 1),
+           "hbm_frac": round(kbytes / (statistics.median(attn_ms) * 1e-3) / 1e9 / hbm_peak, 4),
+           "tflops": round(flops / (med * 1e-3) / 1e12, 2),
+           "tensor_frac": round(flops / (statistics.median(attn_ms) * 1e-3) / 1e12 / tc_peak, 4),
+           "l2": f"{reps} cache replicas rotated"}
+    return rec
+
+
+def run_ours(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(dev)
+    hbm_peak, tc_burst, tc_sust, peak_kind = peaks()
+    spec = W.WORKLOADS[args.workload]
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    reps = n_replicas(spec)
+    inp = W.make(spec, replicas=reps)
+    call = Call(inp, dev)
+    evs, arrs = event_triplets(args.steps)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(stream, replica=i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("timed_start")
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            call(stream, replica=i, events=arrs[i])
+        end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("timed_end")
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    attn_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
+    merge_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+
+    # end-to-end through the public API with host buffers: H2D of the step's inputs from
+    # pinned memory, the call, D2H of the output, all inside the timed region
+    import varlen_gqa_attention_paged_gb300 as ua
+    host = {n: getattr(inp, n).pin_memory() for n in ("q", "cu_seqlens_q", "seq_lens_k")}
+    host_tables = [inp.block_table[r].contiguous().pin_memory() for r in range(reps)] \
+        if inp.block_table.dim() == 3 else [inp.block_table.pin_memory()]
+    out_host = torch.empty(call.out.shape, dtype=call.out.dtype).pin_memory()
+    e2e_steps = max(10, min(args.steps, 500))
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        host_tables[0].numel() * host_tables[0].element_size()
+    d2h = out_host.numel() * out_host.element_size()
+    dq = call.d["q"]
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(e2e_steps):
+            r = i % len(host_tables)
+            dq.copy_(host["q"], non_blocking=True)
+            call.d["cu_seqlens_q"].copy_(host["cu_seqlens_q"], non_blocking=True)
+            call.d["seq_lens_k"].copy_(host["seq_lens_k"], non_blocking=True)
+            call.tables[r % len(call.tables)].copy_(host_tables[r], non_blocking=True)
+            ua.unified_attention(dq, call.d["k_cache"], call.d["v_cache"], call.d["cu_seqlens_q"],
+                                 call.d["seq_lens_k"], call.tables[r % len(call.tables)],
+                                 max_seqlen_q=inp.max_seqlen_q, max_seqlen_k=inp.max_seqlen_k,
+                                 scale=inp.scale, softcap=inp.softcap,
+                                 window_left=inp.window_left, alibi_slopes=call.d["alibi_slopes"],
+                                 qq_bias=call.d["qq_bias"], sinks=call.d["sinks"],
+                                 kv_scale=call.kv_scale, out=call.out, stream=stream)
+            out_host.copy_(call.out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    clocks = sampler.stop() if rank == 0 else None
+
+    extra = {}
+    if rank == 0 and not args.skip_workloads:
+        for name in args.workloads.split(","):
+            if not name or name == args.workload:
+                continue
+            try:
+                w_inp, w_call, w_reps, a_ms, t_ms = measure_workload(
+                    W.WORKLOADS[name], dev, stream, steps=args.workload_steps, warmup=3)
+                extra[name] = workload_record(w_inp, w_call, w_reps, a_ms, t_ms, hbm_peak,
+                                              tc_burst)
+                del w_inp, w_call
+                torch.cuda.empty_cache()
+            except Exception as exc:  # a workload that fails is reported, not hidden
+                extra[name] = {"error": str(exc)[:200]}
+
+    if rank != 0:
+        return
+    tokens_per_step = inp.total_q
+    value = world * tokens_per_step * args.steps / (elapsed_ms * 1e-3)
+    attn_us = statistics.mean(attn_ms) * 1e3
+    kbytes = W.kv_bytes_read(inp)
+    achieved = kbytes / (attn_us * 1e-6) / 1e9
+    kernel_key = f"ua_attn_tile_kernel/{spec.name}"
+    cpu = cpu_baseline(inp, budget_s=args.cpu_seconds)
+    line = {
+        "metric": "decode tokens/s (kernel-level, whole job)",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, shuffled block table)",
+        "config": {"workload": spec.name, "desc": spec.desc, "batch": len(spec.seqs),
+                   "q_len": spec.seqs[0][0], "kv_len": spec.seqs[0][1], "window": spec.window,
+                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+                   "head_dim": spec.head_dim, "block_size": spec.block_size,
+                   "path": "split" if call.plan["path"] == 2 else "2d",
+                   "n_part": call.plan["n_part"],
+                   "l2": f"inputs larger than L2: {reps} cache replicas on disjoint blocks, "
+                         f"step i reads replica i mod {reps}",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": round(kbytes * args.steps / (elapsed_ms * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": recorded_traffic(kernel_key), "peak_source": peak_kind,
+                     "kernel": "ua_attn_tile_kernel (split-KV partition)",
+                     "algorithmic_bytes_per_launch": kbytes,
+                     "kernel_us_mean": round(attn_us, 3),
+                     "merge_us_mean": round(statistics.mean(merge_ms) * 1e3, 3)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * tokens_per_step * e2e_steps / (e2e_ms * 1e-3), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps,
+                "note": "public Python API per step: pinned H2D of q + metadata + block table, "
+                        "call, D2H of out; the KV cache stays resident"},
+        "gpu_launches": call.launches_per_call * args.steps,
+        "clocks": clocks,
+        "workloads": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(inp, budget_s=12.0, sample_seqs=None):
+    """The oracle as it stands, on the host cores, over a bounded sample of the workload."""
+    import oracle
+    threads = os.cpu_count() or 1
+    kw = inp.oracle_kwargs()
+    total_heads = inp.spec.num_q_heads
+    # one sample = every query token of the step for a slice of heads, sized to ~1 s
+    heads = total_heads
+    t0 = time.time()
+    oracle.attention(threads=threads, head_range=(0, 1), **kw)
+    one = max(time.time() - t0, 1e-3)
+    heads = max(1, min(total_heads, int(1.0 / one)))
+    done_tokens = 0.0
+    t0 = time.time()
+    reps = 0
+    while True:
+        oracle.attention(threads=threads, head_range=(0, heads), **kw)
+        reps += 1
+        done_tokens += inp.total_q * heads / total_heads
+        if time.time() - t0 > budget_s or reps >= 1000:
+            break
+    el = time.time() - t0
+    return {"value": round(done_tokens / el, 3), "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reps} x (all {inp.total_q} query tokens, heads 0..{heads - 1} of "
+                      f"{total_heads}) in {el:.1f} s; tokens scaled by heads/{total_heads}"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    spec = W.WORKLOADS[args.workload]
+    inp = W.make(spec)
+    threads = os.cpu_count() or 1
+    kw = inp.oracle_kwargs()
+    total_heads = spec.num_q_heads
+    t0 = time.time()
+    oracle.attention(threads=threads, head_range=(0, 1), **kw)
+    one = max(time.time() - t0, 1e-3)
+    # each step: all query tokens, a slice of heads sized so K+W steps take ~2 minutes
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    heads = max(1, min(total_heads, int(per_step_budget / one)))
+    for _ in range(args.warmup):
+        oracle.attention(threads=threads, head_range=(0, heads), **kw)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.attention(threads=threads, head_range=(0, heads), **kw)
+    el = time.time() - t0
+    tokens = inp.total_q * heads / total_heads * args.steps
+    value = tokens / el
+    sample = (f"each step: all {inp.total_q} query tokens x heads 0..{heads - 1} of "
+              f"{total_heads}; tokens scaled by heads/{total_heads}")
+    line = {"impl": "reference", "metric": "decode tokens/s (kernel-level, whole job)",
+            "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) q/k/v, shuffled block table)",
+            "config": {"workload": spec.name, "desc": spec.desc},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="swdecode_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workloads", default=",".join(W.WORKLOADS),
+                    help="other workloads measured per call and reported under 'workloads'")
+    ap.add_argument("--workload-steps", type=int, default=20)
+    ap.add_argument("--skip-workloads", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,115 @@
+"""The C ABI on the host: the library loads, exports what include/ua.h declares, rejects
+bad arguments before touching the GPU, and the dispatcher plans as designed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import varlen_gqa_attention_paged_gb300 as ua
+from varlen_gqa_attention_paged_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "ua.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(ua_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.load()
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.ua_version() == 100
+    assert lib.ua_status_string(0) == b"ok"
+    assert b"workspace" in lib.ua_status_string(4)
+
+
+FAKE = 0x7f0000001000  # aligned, never dereferenced: every case fails validation first
+
+
+def call(**over):
+    sh = _lib.UaShape()
+    sh.num_seqs, sh.total_q, sh.max_seqlen_q, sh.max_seqlen_k = 2, 6, 5, 37
+    sh.max_blocks_per_seq, sh.num_blocks, sh.q_dtype, sh.out_dtype = 3, 8, 0, 0
+    for k in list(over):
+        if hasattr(sh, k) and k not in ("head_dim",):
+            setattr(sh, k, over.pop(k))
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, cu=FAKE, sl=FAKE, bt=FAKE, block_size=16, hq=4,
+             hkv=2, d=64, scale=0.125, softcap=0.0, wl=-1, alibi=None, qq=None, sinks=None,
+             kv_dtype=0, kv_scale=None, backend=0)
+    a.update(over)
+    v = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return _lib.load().ua_unified_attention(
+        v(a["q"]), v(a["k"]), v(a["v"]), v(a["out"]), v(a["cu"]), v(a["sl"]), v(a["bt"]),
+        a["block_size"], a["hq"], a["hkv"], a["d"], a["scale"], a["softcap"], a["wl"],
+        v(a["alibi"]), v(a["qq"]), v(a["sinks"]), a["kv_dtype"], v(a["kv_scale"]), a["backend"],
+        None, ctypes.byref(sh))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d=96), _lib.UA_ERR_INVALID_ARG),
+    (dict(hq=6, hkv=4), _lib.UA_ERR_INVALID_ARG),
+    (dict(hkv=0), _lib.UA_ERR_INVALID_ARG),
+    (dict(block_size=0), _lib.UA_ERR_INVALID_ARG),
+    (dict(q=None), _lib.UA_ERR_INVALID_ARG),
+    (dict(bt=None), _lib.UA_ERR_INVALID_ARG),
+    (dict(k=FAKE + 8), _lib.UA_ERR_INVALID_ARG),
+    (dict(kv_dtype=7), _lib.UA_ERR_INVALID_ARG),
+    (dict(backend=9), _lib.UA_ERR_INVALID_ARG),
+    (dict(kv_dtype=1), _lib.UA_ERR_UNSUPPORTED),            # f16 q with a bf16 cache
+    (dict(kv_dtype=2), _lib.UA_ERR_INVALID_ARG),            # fp8 cache without kv_scale
+    (dict(qq=FAKE, qq_bias_stride=4), _lib.UA_ERR_INVALID_ARG),   # stride < max_seqlen_q
+    (dict(out_dtype=2), _lib.UA_ERR_INVALID_ARG),
+    (dict(num_blocks=-1), _lib.UA_ERR_INVALID_ARG),
+])
+def test_host_validation_rejects_before_any_launch(over, code):
+    assert call(**over) == code
+
+
+def test_empty_batch_is_a_no_op():
+    assert call(total_q=0) == _lib.UA_OK
+    assert call(num_seqs=0, total_q=0) == _lib.UA_OK
+
+
+def _plan(**kw):
+    base = dict(num_seqs=8, total_q=8, max_seqlen_q=1, max_seqlen_k=6700, block_size=16,
+                num_q_heads=32, num_kv_heads=8, head_dim=128, window_left=4095,
+                kv_dtype=_lib.UA_DT_BF16, num_sms=152, max_blocks_per_seq=419, num_blocks=4190)
+    base.update(kw)
+    return ua.plan(**base)
+
+
+def test_dispatcher_splits_long_underfilled_decode():
+    p = _plan()
+    assert p["path"] == _lib.UA_PATH_SPLIT and p["n_part"] >= 2
+    assert p["block_m"] == 16 and p["grid_y"] == 8 and p["grid_z"] == p["n_part"]
+    assert p["grid_x"] == 8 * 4 // 16 + 8
+    assert p["workspace_bytes"] >= 8 * 32 * p["n_part"] * (128 + 2) * 4
+
+
+def test_dispatcher_keeps_short_or_full_grids_on_2d():
+    # short walk: no split
+    assert _plan(max_seqlen_k=300, window_left=-1)["path"] == _lib.UA_PATH_2D
+    # long prefill: the 2D grid already fills the device
+    p = _plan(num_seqs=5, total_q=18432, max_seqlen_q=4096, max_seqlen_k=18432, window_left=-1)
+    assert p["path"] == _lib.UA_PATH_2D and p["block_m"] >= 64 and p["workspace_bytes"] == 0
+
+
+def test_dispatcher_forced_backends_and_split_count():
+    assert _plan(backend="2d")["n_part"] == 1
+    assert _plan(backend="split", max_seqlen_k=40, window_left=-1)["n_part"] >= 2
+    assert _plan(backend="split", num_splits=5)["n_part"] == 5
+    one = _plan(backend="split", num_splits=5)["workspace_bytes"]
+    assert one > 0
+    assert ua._lib.load().ua_workspace_bytes is not None
+
+
+def test_dispatcher_walk_uses_the_window():
+    # a short window bounds the walk: no split even though kv_len is long
+    assert _plan(window_left=127)["path"] == _lib.UA_PATH_2D

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 CPU oracle.
+
+Every call runs with unused cache slots and blocks poisoned with NaN (e4m3 code
+0x7F), so a read outside the attended keys shows up in the output.  The bar is the
+stated one: max abs error 2e-3 for fp16/bf16 caches and 2e-2 for the fp8 cache, on
+the fp32-output mode; 16-bit outputs may add one unit in the last place of their type.
+"""
+import os
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_gqa_attention_paged_gb300 as ua
+import workloads as W
+from tests._gpu import TOL, max_err, run, to_dev, ulp16
+
+pytestmark = pytest.mark.gpu
+THREADS = min(16, os.cpu_count() or 1)
+
+_ORACLE_CACHE = {}
+
+
+def oracle_out(inp, key):
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = oracle.attention(threads=THREADS, **inp.oracle_kwargs())
+    return _ORACLE_CACHE[key]
+
+
+_INPUT_CACHE = {}
+
+
+def inputs(spec):
+    if spec.name not in _INPUT_CACHE:
+        _INPUT_CACHE[spec.name] = W.make(spec, poison=True)
+    return _INPUT_CACHE[spec.name]
+
+
+FULL = [W.TINY, W.DECODE, W.MIXED, W.SWDECODE_BF16, W.SWDECODE_FP8]
+
+
+@pytest.mark.parametrize("backend", ["auto", "2d", "split"])
+@pytest.mark.parametrize("spec", FULL, ids=lambda s: s.name)
+def test_workload_parity_fp32_out(spec, backend):
+    inp = inputs(spec)
+    want = oracle_out(inp, spec.name)
+    out = run(inp, backend=backend)
+    err = max_err(out, want)
+    assert np.isfinite(out.cpu().numpy()).all()
+    assert err <= TOL[spec.kv_dtype], f"{spec.name}/{backend}: max abs err {err:.3e}"
+
+
+@pytest.mark.parametrize("spec", FULL, ids=lambda s: s.name)
+def test_workload_parity_16bit_out(spec):
+    inp = inputs(spec)
+    want = oracle_out(inp, spec.name)
+    out = run(inp, backend="auto", out_dtype=spec.q_dtype)
+    got = out.cpu().to(torch.float64).numpy()
+    bound = TOL[spec.kv_dtype] + ulp16(want, spec.q_dtype)
+    assert (np.abs(got - want) <= bound).all()
+
+
+@pytest.mark.parametrize("spec", [W.PREFILL_D128, W.PREFILL_D256], ids=lambda s: s.name)
+def test_long_prefill_sampled_rows(spec):
+    """Full-size prefill in the bench's launch configuration; sampled rows vs the oracle."""
+    inp = W.make(spec)
+    out = run(inp, backend="auto").cpu()
+    g = np.random.default_rng(0)
+    cu = inp.cu_seqlens_q.tolist()
+    tok = []
+    for b in range(inp.num_seqs):
+        a, e = cu[b], cu[b + 1]
+        tok += [a, a + 1, e - 1, e - 2] + list(g.integers(a, e, size=6))
+    tok = np.array(tok, dtype=np.int32)
+    heads = g.integers(0, spec.num_q_heads, size=len(tok)).astype(np.int32)
+    want = oracle.attention_rows(tokens=tok, heads=heads, threads=THREADS, **inp.oracle_kwargs())
+    got = out[torch.from_numpy(tok).long(), torch.from_numpy(heads).long()].double().numpy()
+    err = float(np.abs(got - want).max())
+    assert err <= TOL[spec.kv_dtype], f"max abs err {err:.3e}"
+    assert torch.isfinite(out).all()
+
+
+def _small(seed, **kw):
+    base = dict(name=f"s{seed}", seqs=[(1, 37), (5, 18), (17, 80), (0, 9), (1, 1), (3, 300)],
+                num_q_heads=8, num_kv_heads=2, head_dim=128, seed=seed)
+    base.update(kw)
+    return W.Spec(**base)
+
+
+SMALL = {
+    "d64_g4_bs13": dict(head_dim=64, block_size=13, num_q_heads=8, num_kv_heads=2),
+    "d256_g6_window": dict(head_dim=256, num_q_heads=12, num_kv_heads=2, window=33),
+    "mha_bs32": dict(num_q_heads=4, num_kv_heads=4, block_size=32),
+    "g7_bs64_sinks": dict(num_q_heads=7, num_kv_heads=1, block_size=64, sinks=True),
+    "bf16_all_features": dict(q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, softcap=20.0,
+                              alibi=True, qq_bias=True, qq_bias_shape=(32, 64), sinks=True,
+                              window=50),
+    "fp8_f16q_window": dict(kv_dtype=torch.float8_e4m3fn, window=40, sinks=True),
+    "fp8_bf16q_d64": dict(kv_dtype=torch.float8_e4m3fn, q_dtype=torch.bfloat16, head_dim=64),
+    "bs1_g16": dict(block_size=1, num_q_heads=16, num_kv_heads=1),
+    "window1": dict(window=1, sinks=True),
+    "kv_shorter_than_q": dict(seqs=[(4, 2), (1, 0), (6, 6), (2, 40)], sinks=True),
+    "g32_decode": dict(seqs=[(1, 700), (1, 33)], num_q_heads=32, num_kv_heads=1),
+}
+
+
+@pytest.mark.parametrize("backend", ["auto", "2d", "split"])
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_small_cases(case, backend):
+    spec = _small(100 + sorted(SMALL).index(case), **SMALL[case])
+    inp = W.make(spec, poison=True)
+    want = oracle.attention(threads=THREADS, **inp.oracle_kwargs())
+    out = run(inp, backend=backend)
+    err = max_err(out, want)
+    assert err <= TOL[spec.kv_dtype], f"{case}/{backend}: {err:.3e}"
+
+
+@pytest.mark.parametrize("n_part", [2, 3, 7, 16, 64])
+def test_forced_partition_counts(n_part):
+    inp = inputs(W.SWDECODE_BF16)
+    want = oracle_out(inp, W.SWDECODE_BF16.name)
+    out = run(inp, backend="split", num_splits=n_part)
+    assert max_err(out, want) <= 2e-3
+
+
+@pytest.mark.parametrize("kv", [torch.float16, torch.float8_e4m3fn])
+def test_block_table_permutation_is_bit_exact(kv):
+    spec = _small(7, kv_dtype=kv, window=100, sinks=True, num_blocks=80)
+    inp = W.make(spec)
+    base = run(inp, backend="split").cpu()
+    perm = torch.randperm(inp.k_cache.shape[0], generator=torch.Generator().manual_seed(5))
+    k2, v2 = torch.empty_like(inp.k_cache), torch.empty_like(inp.v_cache)
+    k2.view(torch.uint8)[perm] = inp.k_cache.view(torch.uint8)
+    v2.view(torch.uint8)[perm] = inp.v_cache.view(torch.uint8)
+    inp2 = replace(inp, k_cache=k2, v_cache=v2, block_table=perm[inp.block_table.long()].int())
+    for backend in ("split", "2d"):
+        ref = run(inp, backend=backend).cpu()
+        got = run(inp2, backend=backend).cpu()
+        assert torch.equal(ref.view(torch.int32), got.view(torch.int32))
+    assert base.shape == ref.shape
+
+
+def test_e4m3_dequant_of_all_codes_is_exact():
+    """kv_len 1 makes out = V row * v_scale exactly: the device decode of every code."""
+    spec = W.Spec("codes", [(1, 1), (1, 1)], 1, 1, 128, kv_dtype=torch.float8_e4m3fn,
+                  q_dtype=torch.float16, seed=3, num_blocks=2)
+    inp = W.make(spec)
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    v = torch.zeros_like(inp.v_cache.view(torch.uint8))
+    b0, b1 = int(inp.block_table[0, 0]), int(inp.block_table[1, 0])
+    v[b0, 0, 0] = codes[:128]
+    v[b1, 0, 0] = codes[128:]
+    inp.v_cache = v.view(torch.float8_e4m3fn)
+    inp.k_scale, inp.v_scale = 1.0, 1.0
+    out = run(inp, backend="2d").cpu().double().numpy().reshape(-1)
+    want = oracle.decode(codes.numpy(), oracle.E4M3)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(out), nan)
+    assert np.array_equal(out[~nan], want[~nan])
+
+
+def test_two_streams_share_nothing():
+    a, b = inputs(W.SWDECODE_BF16), inputs(W.DECODE)
+    da, db = to_dev(a), to_dev(b)
+    wa, wb = oracle_out(a, W.SWDECODE_BF16.name), oracle_out(b, W.DECODE.name)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            oa = run(a, backend="split", dev_inputs=da)
+        with torch.cuda.stream(s2):
+            ob = run(b, backend="split", dev_inputs=db)
+        outs.append((oa, ob))
+    torch.cuda.synchronize()
+    for oa, ob in outs:
+        assert max_err(oa, wa) <= 2e-3 and max_err(ob, wb) <= 2e-3
+
+
+def test_library_workspace_reuse_across_head_sizes():
+    for d in (64, 128, 256, 64):
+        spec = _small(20 + d, head_dim=d, seqs=[(1, 900), (2, 1500)], sinks=True)
+        inp = W.make(spec, poison=True)
+        want = oracle.attention(threads=THREADS, **inp.oracle_kwargs())
+        assert max_err(run(inp, backend="split", num_splits=9), want) <= 2e-3
+
+
+def test_caller_workspace_and_too_small_workspace():
+    inp = inputs(W.SWDECODE_BF16)
+    want = oracle_out(inp, W.SWDECODE_BF16.name)
+    need = ua.plan(num_seqs=inp.num_seqs, total_q=inp.total_q, max_seqlen_q=inp.max_seqlen_q,
+                   max_seqlen_k=inp.max_seqlen_k, block_size=16, num_q_heads=32,
+                   num_kv_heads=8, head_dim=128, window_left=inp.window_left,
+                   kv_dtype=ua.UA_DT_BF16, backend="split")["workspace_bytes"]
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN-filled scratch
+    assert max_err(run(inp, backend="split", workspace=ws), want) <= 2e-3
+    with pytest.raises(ua.UaError) as e:
+        run(inp, backend="split", workspace=ws[: need - 256])
+    assert e.value.code == ua._lib.UA_ERR_WORKSPACE
+
+
+def test_out_of_range_block_id_is_reported_not_read():
+    inp = W.make(_small(9))
+    bt = inp.block_table.clone()
+    bt[2, 1] = 10 ** 6
+    inp2 = replace(inp, block_table=bt)
+    ua.device_status_reset()
+    out = run(inp2, backend="2d")
+    assert ua.device_status() == ua._lib.UA_ERR_DEVICE_CHECK
+    ua.device_status_reset()
+    assert ua.device_status() == 0
+    assert torch.isfinite(out).all()

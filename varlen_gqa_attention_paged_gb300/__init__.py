@@ -1,0 +1,154 @@
+"""Unified paged varlen GQA attention for GB300 (sm_103a).
+
+Python binding of the C ABI in ``include/ua.h``: it only turns torch tensors into
+device pointers, the current CUDA stream and host-side sizes, and calls
+``ua_unified_attention`` in ``libua.so``.  Every step of the computation runs in the
+library's CUDA kernels; without the built library this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import (UA_BACKEND_2D, UA_BACKEND_AUTO, UA_BACKEND_SPLIT, UA_DT_BF16, UA_DT_F8E4M3,
+                   UA_DT_F16, UA_DT_F32, UA_PATH_2D, UA_PATH_SPLIT)
+
+__all__ = ["unified_attention", "plan", "device_status", "device_status_reset", "UaError",
+           "BACKENDS", "library_path"]
+
+BACKENDS = {"auto": UA_BACKEND_AUTO, "2d": UA_BACKEND_2D, "split": UA_BACKEND_SPLIT}
+_DTYPES = {torch.float16: UA_DT_F16, torch.bfloat16: UA_DT_BF16,
+           torch.float8_e4m3fn: UA_DT_F8E4M3, torch.float32: UA_DT_F32}
+
+
+class UaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        lib = _lib.load()
+        super().__init__(f"{what}: {lib.ua_status_string(code).decode()} (status {code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _shape(q, k_cache, block_table, cu_seqlens_q, max_seqlen_q, max_seqlen_k, qq_bias,
+           out_dtype_code, num_splits, workspace, events):
+    sh = _lib.UaShape()
+    sh.num_seqs = cu_seqlens_q.numel() - 1
+    sh.total_q = q.shape[0]
+    sh.max_seqlen_q = int(max_seqlen_q)
+    sh.max_seqlen_k = int(max_seqlen_k)
+    sh.max_blocks_per_seq = block_table.shape[-1]
+    sh.num_blocks = k_cache.shape[0]
+    sh.qq_bias_stride = qq_bias.shape[-1] if qq_bias is not None else 0
+    sh.q_dtype = _dtype_code(q)
+    sh.out_dtype = out_dtype_code
+    sh.num_splits = int(num_splits)
+    if workspace is not None:
+        sh.workspace = workspace.data_ptr()
+        sh.workspace_bytes = workspace.numel() * workspace.element_size()
+    if events is not None:
+        arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+        sh.events = ctypes.cast(arr, ctypes.c_void_p)
+        sh._events_keepalive = arr  # noqa: SLF001 -- keep the array alive for the call
+    return sh
+
+
+def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *,
+                      max_seqlen_q: int, max_seqlen_k: int, scale: float | None = None,
+                      softcap: float = 0.0, window_left: int = -1, alibi_slopes=None,
+                      qq_bias=None, sinks=None, kv_scale=None, out=None, out_dtype=None,
+                      backend: str = "auto", num_splits: int = 0, workspace=None, stream=None,
+                      events=None):
+    """Paged varlen GQA attention on the GPU; returns ``out`` [total_q, H_q, D].
+
+    q [total_q, H_q, D] f16/bf16; k_cache, v_cache [num_blocks, block_size, H_kv, D]
+    f16/bf16/float8_e4m3fn; cu_seqlens_q [S+1], seq_lens_k [S], block_table [S, max_blocks]
+    int32; alibi_slopes / sinks [H_q] and qq_bias [rows, stride] float32; kv_scale float32[2]
+    (k_scale, v_scale) for the fp8 cache.  max_seqlen_q / max_seqlen_k are host ints.
+    """
+    lib = _lib.load()
+    total_q, hq, d = q.shape
+    num_blocks, block_size, hkv, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape:
+        raise ValueError("q, k_cache and v_cache disagree on shape")
+    if qq_bias is not None and qq_bias.shape[0] < max_seqlen_q:
+        raise ValueError("qq_bias needs at least max_seqlen_q rows")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens_k", seq_lens_k),
+                    ("block_table", block_table)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    if not (q.is_cuda and k_cache.is_cuda and v_cache.is_cuda):
+        raise ValueError("q, k_cache and v_cache must be CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sh = _shape(q, k_cache, block_table, cu_seqlens_q, max_seqlen_q, max_seqlen_k, qq_bias,
+                _dtype_code(out), num_splits, workspace, events)
+    rc = lib.ua_unified_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(cu_seqlens_q), _ptr(seq_lens_k),
+        _ptr(block_table), block_size, hq, hkv, d, float(scale), float(softcap or 0.0),
+        int(window_left if window_left is not None else -1), _ptr(alibi_slopes), _ptr(qq_bias),
+        _ptr(sinks), _dtype_code(k_cache), _ptr(kv_scale), BACKENDS[backend],
+        ctypes.c_void_p(stream.cuda_stream), ctypes.byref(sh))
+    if rc != 0:
+        raise UaError(rc, "ua_unified_attention")
+    return out
+
+
+def plan(*, num_seqs, total_q, max_seqlen_q, max_seqlen_k, block_size, num_q_heads,
+         num_kv_heads, head_dim, window_left=-1, kv_dtype=UA_DT_BF16, q_dtype=None,
+         backend="auto", num_splits=0, num_sms=0, max_blocks_per_seq=1, num_blocks=1):
+    """The dispatcher's decision for these sizes (host only; no GPU needed when num_sms > 0)."""
+    lib = _lib.load()
+    sh = _lib.UaShape()
+    sh.num_seqs, sh.total_q = num_seqs, total_q
+    sh.max_seqlen_q, sh.max_seqlen_k = max_seqlen_q, max_seqlen_k
+    sh.max_blocks_per_seq, sh.num_blocks = max_blocks_per_seq, num_blocks
+    sh.q_dtype = q_dtype if q_dtype is not None else (UA_DT_BF16 if kv_dtype == UA_DT_F8E4M3
+                                                      else kv_dtype)
+    sh.out_dtype = sh.q_dtype
+    sh.num_splits = num_splits
+    pl = _lib.UaPlan()
+    rc = lib.ua_plan(ctypes.byref(sh), block_size, num_q_heads, num_kv_heads, head_dim,
+                     window_left, kv_dtype, BACKENDS[backend], num_sms, ctypes.byref(pl))
+    if rc != 0:
+        raise UaError(rc, "ua_plan")
+    return {f: getattr(pl, f) for f, _ in pl._fields_}
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return the kernels' device check status (ua_status_t)."""
+    lib = _lib.load()
+    stream = stream or torch.cuda.current_stream()
+    st = ctypes.c_int(0)
+    rc = lib.ua_device_status(ctypes.c_void_p(stream.cuda_stream), ctypes.byref(st))
+    if rc != 0:
+        raise UaError(rc, "ua_device_status")
+    return st.value
+
+
+def device_status_reset(stream=None) -> None:
+    lib = _lib.load()
+    stream = stream or torch.cuda.current_stream()
+    rc = lib.ua_device_status_reset(ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise UaError(rc, "ua_device_status_reset")

@@ -1,0 +1,329 @@
+// ua_api.cu -- C ABI of libua.so: argument checks, the dispatcher (2D vs split-KV from
+// grid fill and key-walk length), the split workspace, and the kernel launches.
+#include <algorithm>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "ua.h"
+#include "ua_internal.h"
+
+namespace {
+
+__device__ unsigned int g_device_status = 0;
+
+// Keys per split partition below which splitting a q-block's walk does not pay: the
+// partition must amortise its prologue and the extra merge traffic.
+constexpr int kMinPartitionKeys = 256;
+// CTAs of the tile kernel resident per SM (shared-memory bound: one 160-thread CTA).
+constexpr int kTileCtasPerSm = 1;
+constexpr int kMaxPartitions = 128;
+
+int device_sm_count(int* out) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it == cache.end()) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return UA_ERR_CUDA;
+    it = cache.emplace(dev, n).first;
+  }
+  *out = it->second;
+  return UA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int kv_dtype,
+                int backend) {
+  if (sh == nullptr) return UA_ERR_INVALID_ARG;
+  if (sh->num_seqs < 0 || sh->total_q < 0 || sh->max_seqlen_q < 0 || sh->max_seqlen_k < 0 ||
+      sh->max_blocks_per_seq < 0 || sh->num_blocks < 0 || sh->num_splits < 0)
+    return UA_ERR_INVALID_ARG;
+  if (block_size < 1 || hq < 1 || hkv < 1 || hq % hkv != 0) return UA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return UA_ERR_INVALID_ARG;
+  if (kv_dtype != UA_DT_F16 && kv_dtype != UA_DT_BF16 && kv_dtype != UA_DT_F8E4M3)
+    return UA_ERR_INVALID_ARG;
+  if (sh->q_dtype != UA_DT_F16 && sh->q_dtype != UA_DT_BF16) return UA_ERR_INVALID_ARG;
+  if (sh->out_dtype != UA_DT_F16 && sh->out_dtype != UA_DT_BF16 && sh->out_dtype != UA_DT_F32)
+    return UA_ERR_INVALID_ARG;
+  if (backend != UA_BACKEND_AUTO && backend != UA_BACKEND_2D && backend != UA_BACKEND_SPLIT)
+    return UA_ERR_INVALID_ARG;
+  if (kv_dtype != UA_DT_F8E4M3 && sh->q_dtype != kv_dtype) return UA_ERR_UNSUPPORTED;
+  return UA_OK;
+}
+
+void make_plan(const ua_shape_t* sh, int hq, int hkv, int d, int window_left, int backend,
+               int num_sms, ua_plan_t* pl) {
+  const int group = hq / hkv;
+  const long long rows_max = static_cast<long long>(sh->max_seqlen_q) * group;
+  const int wm = rows_max <= 16 ? 1 : 4;
+  const int bm = ua::tile_block_m(wm);
+  const long long slots = static_cast<long long>(sh->total_q) * group / bm + sh->num_seqs;
+  const long long ctas_2d = slots * hkv;
+  // Longest key walk of one q-block: a window bounds it, otherwise the longest sequence.
+  long long walk = sh->max_seqlen_k;
+  if (window_left >= 0)
+    walk = std::min<long long>(walk, static_cast<long long>(window_left) + 1 + (bm + group - 1) / group);
+  const long long target = static_cast<long long>(num_sms) * kTileCtasPerSm;
+  int n_part = 1;
+  if (backend == UA_BACKEND_SPLIT) {
+    if (sh->num_splits > 0) {
+      n_part = sh->num_splits;
+    } else {
+      long long want = std::max<long long>(2, (target + ctas_2d - 1) / std::max<long long>(1, ctas_2d));
+      want = std::min<long long>(want, std::max<long long>(2, (walk + kMinPartitionKeys - 1) / kMinPartitionKeys));
+      n_part = static_cast<int>(want);
+    }
+  } else if (backend == UA_BACKEND_AUTO) {
+    if (ctas_2d < target && walk >= 2LL * kMinPartitionKeys) {
+      long long want = (target + ctas_2d - 1) / std::max<long long>(1, ctas_2d);
+      want = std::min<long long>(want, walk / kMinPartitionKeys);
+      n_part = static_cast<int>(std::max<long long>(1, want));
+    }
+  }
+  n_part = std::min(n_part, kMaxPartitions);
+  pl->path = n_part > 1 ? UA_PATH_SPLIT : UA_PATH_2D;
+  pl->kernel = wm;
+  pl->block_m = bm;
+  pl->n_part = n_part;
+  pl->grid_x = static_cast<int32_t>(slots);
+  pl->grid_y = hkv;
+  pl->grid_z = n_part;
+  pl->num_sms = num_sms;
+  pl->workspace_bytes = 0;
+  if (n_part > 1) {
+    const size_t rows = static_cast<size_t>(sh->total_q) * hq * n_part;
+    // m and l, then acc; each piece rounded to 256 bytes
+    const size_t ml = ((rows * sizeof(float) + 255) / 256) * 256;
+    const size_t acc = ((rows * d * sizeof(float) + 255) / 256) * 256;
+    pl->workspace_bytes = 2 * ml + acc;
+  }
+}
+
+// Library-owned split workspace: one grow-only buffer per (device, stream).  A buffer
+// that is replaced stays allocated, because earlier work (or a captured graph) on that
+// stream may still use it.
+struct WorkspacePool {
+  std::mutex mu;
+  std::map<std::pair<int, void*>, std::pair<void*, size_t>> live;
+  std::vector<void*> retired;
+};
+
+WorkspacePool& pool() {
+  static WorkspacePool* p = new WorkspacePool();  // never destroyed: kernels may outlive exit order
+  return *p;
+}
+
+int library_workspace(void* stream, size_t bytes, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
+  WorkspacePool& wp = pool();
+  std::lock_guard<std::mutex> lock(wp.mu);
+  auto key = std::make_pair(dev, stream);
+  auto it = wp.live.find(key);
+  if (it != wp.live.end() && it->second.second >= bytes) {
+    *out = it->second.first;
+    return UA_OK;
+  }
+  size_t grow = 1 << 20;
+  while (grow < bytes) grow <<= 1;
+  void* ptr = nullptr;
+  if (cudaMalloc(&ptr, grow) != cudaSuccess) return UA_ERR_CUDA;
+  if (it != wp.live.end()) {
+    wp.retired.push_back(it->second.first);
+    it->second = std::make_pair(ptr, grow);
+  } else {
+    wp.live.emplace(key, std::make_pair(ptr, grow));
+  }
+  *out = ptr;
+  return UA_OK;
+}
+
+int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
+            const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, const int32_t* block_table,
+            int block_size, int hq, int hkv, int d, float scale, float softcap, int window_left,
+            const float* alibi, const float* qq_bias, const float* sinks, int kv_dtype,
+            const float* kv_scale, int backend, void* stream, const ua_shape_t* sh) {
+  int rc = check_sizes(sh, block_size, hq, hkv, d, kv_dtype, backend);
+  if (rc != UA_OK) return rc;
+  if (sh->total_q == 0 || sh->num_seqs == 0) return UA_OK;
+  if (!q || !k_cache || !v_cache || !out || !cu_seqlens_q || !seq_lens_k || !block_table)
+    return UA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return UA_ERR_INVALID_ARG;
+  if (kv_dtype == UA_DT_F8E4M3 && kv_scale == nullptr) return UA_ERR_INVALID_ARG;
+  if (qq_bias != nullptr && sh->qq_bias_stride < std::max(1, sh->max_seqlen_q))
+    return UA_ERR_INVALID_ARG;
+  if (sh->max_blocks_per_seq < 1 || sh->num_blocks < 1) return UA_ERR_INVALID_ARG;
+
+  int num_sms = 0;
+  if ((rc = device_sm_count(&num_sms)) != UA_OK) return rc;
+  ua_plan_t pl;
+  make_plan(sh, hq, hkv, d, window_left, backend, num_sms, &pl);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  ua::AttnParams p{};
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.out = out;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.seq_lens_k = seq_lens_k;
+  p.block_table = block_table;
+  p.alibi = alibi;
+  p.qq_bias = qq_bias;
+  p.sinks = sinks;
+  p.kv_scale = kv_scale;
+  p.num_seqs = sh->num_seqs;
+  p.total_q = sh->total_q;
+  p.max_seqlen_q = sh->max_seqlen_q;
+  p.max_blocks_per_seq = sh->max_blocks_per_seq;
+  p.num_blocks = sh->num_blocks;
+  p.block_size = block_size;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.group = hq / hkv;
+  p.qq_stride = sh->qq_bias_stride;
+  p.window_left = window_left < 0 ? -1 : window_left;
+  p.n_part = pl.n_part;
+  p.q_dtype = sh->q_dtype;
+  p.out_dtype = sh->out_dtype;
+  p.scale = scale;
+  p.softcap = softcap > 0.f ? softcap : 0.f;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
+    return UA_ERR_CUDA;
+
+  if (pl.n_part > 1) {
+    void* ws = sh->workspace;
+    if (ws != nullptr) {
+      if (sh->workspace_bytes < pl.workspace_bytes || !aligned16(ws)) return UA_ERR_WORKSPACE;
+    } else if ((rc = library_workspace(stream, pl.workspace_bytes, &ws)) != UA_OK) {
+      return rc;
+    }
+    const size_t rows = static_cast<size_t>(sh->total_q) * hq * pl.n_part;
+    const size_t ml = ((rows * sizeof(float) + 255) / 256) * 256;
+    p.ws_m = static_cast<float*>(ws);
+    p.ws_l = reinterpret_cast<float*>(static_cast<char*>(ws) + ml);
+    p.ws_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ml);
+  }
+
+  const int kv = kv_dtype == UA_DT_F16 ? ua::KV_F16 : kv_dtype == UA_DT_BF16 ? ua::KV_BF16 : ua::KV_E4M3;
+  const bool feat = softcap > 0.f || alibi != nullptr || qq_bias != nullptr;
+  const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
+  cudaEvent_t* ev = static_cast<cudaEvent_t*>(sh->events);
+  if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return UA_ERR_CUDA;
+  cudaError_t err;
+  switch (d) {
+    case 64: err = ua::launch_tile_d64(p, grid, pl.kernel, kv, feat, st); break;
+    case 128: err = ua::launch_tile_d128(p, grid, pl.kernel, kv, feat, st); break;
+    default: err = ua::launch_tile_d256(p, grid, pl.kernel, kv, feat, st); break;
+  }
+  if (err != cudaSuccess) return UA_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[1], st) != cudaSuccess) return UA_ERR_CUDA;
+  if (pl.n_part > 1) {
+    ua::MergeParams mp{};
+    mp.ws_m = p.ws_m;
+    mp.ws_l = p.ws_l;
+    mp.ws_acc = p.ws_acc;
+    mp.out = out;
+    mp.rows = sh->total_q * hq;
+    mp.n_part = pl.n_part;
+    mp.head_dim = d;
+    mp.out_dtype = sh->out_dtype;
+    if (ua::launch_merge(mp, st) != cudaSuccess) return UA_ERR_CUDA;
+  }
+  if (ev && cudaEventRecord(ev[2], st) != cudaSuccess) return UA_ERR_CUDA;
+  return UA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ua_unified_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
+                         const int32_t* cu_seqlens_q, const int32_t* seq_lens_k,
+                         const int32_t* block_table, int block_size, int num_q_heads,
+                         int num_kv_heads, int head_dim, float scale, float softcap,
+                         int window_left, const float* alibi_slopes, const float* qq_bias,
+                         const float* sinks, int kv_dtype, const float* kv_scale, int backend,
+                         void* stream, const ua_shape_t* shape) {
+  try {
+    return enqueue(q, k_cache, v_cache, out, cu_seqlens_q, seq_lens_k, block_table, block_size,
+                   num_q_heads, num_kv_heads, head_dim, scale, softcap, window_left, alibi_slopes,
+                   qq_bias, sinks, kv_dtype, kv_scale, backend, stream, shape);
+  } catch (...) {
+    return UA_ERR_CUDA;
+  }
+}
+
+int ua_plan(const ua_shape_t* shape, int block_size, int num_q_heads, int num_kv_heads,
+            int head_dim, int window_left, int kv_dtype, int backend, int num_sms,
+            ua_plan_t* plan) {
+  try {
+    if (plan == nullptr) return UA_ERR_INVALID_ARG;
+    int rc = check_sizes(shape, block_size, num_q_heads, num_kv_heads, head_dim, kv_dtype, backend);
+    if (rc != UA_OK) return rc;
+    if (num_sms <= 0 && (rc = device_sm_count(&num_sms)) != UA_OK) return rc;
+    make_plan(shape, num_q_heads, num_kv_heads, head_dim, window_left, backend, num_sms, plan);
+    return UA_OK;
+  } catch (...) {
+    return UA_ERR_CUDA;
+  }
+}
+
+size_t ua_workspace_bytes(const ua_shape_t* shape, int block_size, int num_q_heads,
+                          int num_kv_heads, int head_dim, int window_left, int kv_dtype,
+                          int backend) {
+  ua_plan_t pl;
+  if (ua_plan(shape, block_size, num_q_heads, num_kv_heads, head_dim, window_left, kv_dtype,
+              backend, 0, &pl) != UA_OK)
+    return 0;
+  return pl.workspace_bytes;
+}
+
+int ua_device_status(void* stream, int* status) {
+  if (status == nullptr) return UA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return UA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_status, sizeof(word)) != cudaSuccess) return UA_ERR_CUDA;
+  *status = (word & ua::DEV_BAD_BLOCK) ? UA_ERR_DEVICE_CHECK
+            : (word & ua::DEV_TIMEOUT) ? UA_ERR_TIMEOUT
+                                       : UA_OK;
+  return UA_OK;
+}
+
+int ua_device_status_reset(void* stream) {
+  const unsigned int zero = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) !=
+      cudaSuccess)
+    return UA_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? UA_OK : UA_ERR_CUDA;
+}
+
+const char* ua_status_string(int status) {
+  switch (status) {
+    case UA_OK: return "ok";
+    case UA_ERR_INVALID_ARG: return "invalid argument";
+    case UA_ERR_UNSUPPORTED: return "unsupported combination";
+    case UA_ERR_CUDA: return "CUDA runtime error";
+    case UA_ERR_WORKSPACE: return "workspace too small";
+    case UA_ERR_DEVICE_CHECK: return "device check failed: block id outside the cache";
+    case UA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int ua_version(void) { return UA_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// ua_internal.h -- definitions shared by the host dispatcher and the kernels of libua.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace ua {
+
+enum KvKind { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
+
+// Bits of the device status word (OR-ed by kernels, read by ua_device_status).
+enum : unsigned { DEV_BAD_BLOCK = 1u, DEV_TIMEOUT = 2u };
+
+// Everything one launch of the attention tile kernel needs (passed by value).
+struct AttnParams {
+  const void* q;                // [total_q, hq, D]
+  const void* k;                // [num_blocks, block_size, hkv, D]
+  const void* v;
+  void* out;                    // [total_q, hq, D]          (n_part == 1)
+  const int32_t* cu_seqlens_q;  // [num_seqs + 1]
+  const int32_t* seq_lens_k;    // [num_seqs]
+  const int32_t* block_table;   // [num_seqs, max_blocks_per_seq]
+  const float* alibi;           // [hq] or null
+  const float* qq_bias;         // [*, qq_stride] or null
+  const float* sinks;           // [hq] or null
+  const float* kv_scale;        // {k_scale, v_scale} (fp8 cache) or null
+  float* ws_m;                  // [total_q, hq, n_part]     (n_part > 1)
+  float* ws_l;                  // [total_q, hq, n_part]
+  float* ws_acc;                // [total_q, hq, n_part, D]
+  unsigned int* status;         // device status word
+  int num_seqs, total_q, max_seqlen_q, max_blocks_per_seq, num_blocks, block_size;
+  int hq, hkv, group;
+  int qq_stride, window_left, n_part;
+  int q_dtype, out_dtype;
+  float scale, softcap;
+};
+
+// The LSE-merge of split partitions (one output row per query token x head).
+struct MergeParams {
+  const float* ws_m;
+  const float* ws_l;
+  const float* ws_acc;
+  void* out;
+  int rows;        // total_q * hq
+  int n_part;
+  int head_dim;
+  int out_dtype;
+};
+
+// Rows (query token x head of one kv group) per CTA of the tile kernel.
+constexpr int tile_block_m(int wm) { return 16 * wm; }
+
+cudaError_t launch_tile_d64(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
+                            cudaStream_t s);
+cudaError_t launch_tile_d128(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
+                             cudaStream_t s);
+cudaError_t launch_tile_d256(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
+                             cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+
+}  // namespace ua
