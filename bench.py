@@ -199,6 +199,10 @@ class Call:
 
 def event_triplets(n):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for trip in evs:  # torch creates the CUDA event lazily, on its first record
+        for e in trip:
+            e.record()
+    torch.cuda.synchronize()
     arrs = [(ctypes.c_void_p * 3)(*[e.cuda_event for e in trip]) for trip in evs]
     return evs, arrs
 
@@ -281,10 +285,18 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         start.record(stream)
         for i in range(args.steps):
-            call(stream, replica=i, events=arrs[i])
+            call(stream, replica=i)
         end.record(stream)
     torch.cuda.synchronize()
     sampler.mark("timed_end")
+    # Kernel-timing pass: the same K steps again, with the library's events recorded
+    # around the attention kernel and the merge kernel of every step.  (Events between
+    # the kernels stop them overlapping through programmatic dependent launch, so this
+    # pass is kept out of the timed region above.)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            call(stream, replica=i, events=arrs[i])
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(end)
@@ -383,6 +395,8 @@ def run_ours(args):
                      "kernel": "ua_attn_tile_kernel (split-KV partition)",
                      "algorithmic_bytes_per_launch": kbytes,
                      "kernel_us_mean": round(attn_us, 3),
+                     "kernel_timing": "CUDA events around the attention kernel, every step of "
+                                      "a pass of the same K steps right after the timed region",
                      "merge_us_mean": round(statistics.mean(merge_ms) * 1e3, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * tokens_per_step * e2e_steps / (e2e_ms * 1e-3), 1),

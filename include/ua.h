@@ -104,10 +104,13 @@ typedef struct {
                           q-blocks), 4: tile kernel with 64 rows per CTA */
   int32_t block_m;     /* (query token x head) rows per q-block */
   int32_t n_part;      /* key-range partitions (1 on the 2D path) */
-  int32_t grid_x;      /* q-block slots = floor(total_q * G / block_m) + num_seqs */
+  int32_t grid_x;      /* q-block slots: num_seqs when slot_per_seq, else
+                          floor(total_q * G / block_m) + num_seqs */
   int32_t grid_y;      /* num_kv_heads */
   int32_t grid_z;      /* n_part */
   int32_t num_sms;     /* SM count the plan was made for */
+  int32_t cluster_y;   /* CTAs of one q-block slot (different kv-heads) launched as a cluster */
+  int32_t slot_per_seq; /* 1: every sequence fits one q-block and grid slot x is sequence x */
   size_t workspace_bytes; /* scratch the split path needs (0 on the 2D path) */
 } ua_plan_t;
 
@@ -163,7 +166,8 @@ size_t ua_workspace_bytes(const ua_shape_t* shape, int block_size, int num_q_hea
 /*
  * ua_device_status -- synchronises `stream`, then stores in *status the device
  * check word the kernels of this library raised since the last reset, mapped to
- * UA_OK, UA_ERR_DEVICE_CHECK (a block id outside the cache) or UA_ERR_TIMEOUT (a
+ * UA_OK, UA_ERR_DEVICE_CHECK (a block id outside the cache, or a q_len
+ * above max_seqlen_q in a decode-shaped call) or UA_ERR_TIMEOUT (a
  * bounded wait expired).  Returns UA_OK or UA_ERR_CUDA / UA_ERR_INVALID_ARG.
  */
 int ua_device_status(void* stream, int* status);

@@ -89,13 +89,13 @@ def test_dispatcher_splits_long_underfilled_decode():
     p = _plan()
     assert p["path"] == _lib.UA_PATH_SPLIT and p["n_part"] >= 2
     assert p["block_m"] == 16 and p["grid_y"] == 8 and p["grid_z"] == p["n_part"]
-    assert p["grid_x"] == 8 * 4 // 16 + 8
+    assert p["grid_x"] == 8 and p["slot_per_seq"] == 1 and p["cluster_y"] == 8
     assert p["workspace_bytes"] >= 8 * 32 * p["n_part"] * (128 + 2) * 4
 
 
 def test_dispatcher_keeps_short_or_full_grids_on_2d():
-    # short walk: no split
-    assert _plan(max_seqlen_k=300, window_left=-1)["path"] == _lib.UA_PATH_2D
+    # short walk (below two minimum partitions of 128 keys): no split
+    assert _plan(max_seqlen_k=200, window_left=-1)["path"] == _lib.UA_PATH_2D
     # long prefill: the 2D grid already fills the device
     p = _plan(num_seqs=5, total_q=18432, max_seqlen_q=4096, max_seqlen_k=18432, window_left=-1)
     assert p["path"] == _lib.UA_PATH_2D and p["block_m"] >= 64 and p["workspace_bytes"] == 0
@@ -113,3 +113,20 @@ def test_dispatcher_forced_backends_and_split_count():
 def test_dispatcher_walk_uses_the_window():
     # a short window bounds the walk: no split even though kv_len is long
     assert _plan(window_left=127)["path"] == _lib.UA_PATH_2D
+
+
+def test_dispatcher_split_fits_one_wave():
+    for hkv, seqs, kv in ((8, 8, 1), (2, 4, 0), (8, 2, 2), (1, 1, 1)):
+        p = _plan(num_seqs=seqs, total_q=seqs, num_kv_heads=hkv, num_q_heads=4 * hkv, kv_dtype=kv,
+                  window_left=-1, max_seqlen_k=100000)
+        active = seqs * hkv
+        assert p["path"] == _lib.UA_PATH_SPLIT
+        assert active * p["n_part"] <= 2 * 152            # two CTAs per SM at most
+        # the largest count that fits: one more partition would start a second wave
+        assert active * (p["n_part"] + 1) > 2 * 152 or p["n_part"] == 128
+
+
+def test_dispatcher_mixed_batch_splits_underfilled_long_walks():
+    p = _plan(num_seqs=5, total_q=327, max_seqlen_q=129, max_seqlen_k=1328, num_q_heads=16,
+              num_kv_heads=2, window_left=-1)
+    assert p["path"] == _lib.UA_PATH_SPLIT and p["n_part"] >= 2 and p["slot_per_seq"] == 0

@@ -63,6 +63,9 @@ def _shape(q, k_cache, block_table, cu_seqlens_q, max_seqlen_q, max_seqlen_k, qq
         sh.workspace = workspace.data_ptr()
         sh.workspace_bytes = workspace.numel() * workspace.element_size()
     if events is not None:
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event lazily, on its first record
+                e.record()
         arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
         sh.events = ctypes.cast(arr, ctypes.c_void_p)
         sh._events_keepalive = arr  # noqa: SLF001 -- keep the array alive for the call

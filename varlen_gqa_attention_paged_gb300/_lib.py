@@ -50,6 +50,8 @@ class UaPlan(ctypes.Structure):
         ("grid_y", ctypes.c_int32),
         ("grid_z", ctypes.c_int32),
         ("num_sms", ctypes.c_int32),
+        ("cluster_y", ctypes.c_int32),
+        ("slot_per_seq", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_size_t),
     ]
 

@@ -1,13 +1,16 @@
 // ua_api.cu -- C ABI of libua.so: argument checks, the dispatcher (2D vs split-KV from
 // grid fill and key-walk length), the split workspace, and the kernel launches.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <map>
 #include <mutex>
 #include <utility>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "ua.h"
 #include "ua_internal.h"
@@ -18,9 +21,7 @@ __device__ unsigned int g_device_status = 0;
 
 // Keys per split partition below which splitting a q-block's walk does not pay: the
 // partition must amortise its prologue and the extra merge traffic.
-constexpr int kMinPartitionKeys = 256;
-// CTAs of the tile kernel resident per SM (shared-memory bound: one 160-thread CTA).
-constexpr int kTileCtasPerSm = 1;
+constexpr int kMinPartitionKeys = 128;
 constexpr int kMaxPartitions = 128;
 
 int device_sm_count(int* out) {
@@ -42,6 +43,47 @@ int device_sm_count(int* out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// A paged cache [num_blocks * block_size][H_kv][D] as a 3-D TMA tensor; one box is 16
+// cache rows of one kv-head and one column block (128 bytes, swizzled; 64-byte rows
+// unswizzled).  Rows past the tensor read as zero.
+bool encode_cache_map(CUtensorMap* map, const void* base, int kv_dtype, int num_blocks,
+                      int block_size, int hkv, int d) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const int esz = kv_dtype == UA_DT_F8E4M3 ? 1 : 2;
+  const int row_bytes = d * esz;
+  const int cbw = row_bytes >= 128 ? 128 : row_bytes;
+  const CUtensorMapDataType dt = kv_dtype == UA_DT_F8E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : kv_dtype == UA_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(num_blocks) * block_size};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(row_bytes) * hkv};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(cbw / esz), 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         cbw == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int kv_dtype,
                 int backend) {
   if (sh == nullptr) return UA_ERR_INVALID_ARG;
@@ -61,34 +103,34 @@ int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, in
   return UA_OK;
 }
 
-void make_plan(const ua_shape_t* sh, int hq, int hkv, int d, int window_left, int backend,
-               int num_sms, ua_plan_t* pl) {
+// The dispatcher.  Split the key walk (UA_BACKEND_AUTO) only when the 2D grid leaves
+// part of one wave of SMs idle and the walk spans at least two minimum partitions;
+// then into as many partitions as still fit in that one wave (at least two): a
+// second, partly filled wave costs more than the extra parallelism gives back.
+void make_plan(const ua_shape_t* sh, int hq, int hkv, int d, int window_left, int kv_dtype,
+               int backend, int num_sms, ua_plan_t* pl) {
   const int group = hq / hkv;
   const long long rows_max = static_cast<long long>(sh->max_seqlen_q) * group;
   const int wm = rows_max <= 16 ? 1 : 4;
   const int bm = ua::tile_block_m(wm);
-  const long long slots = static_cast<long long>(sh->total_q) * group / bm + sh->num_seqs;
-  const long long ctas_2d = slots * hkv;
+  // every sequence fits one q-block: slot x is sequence x; else the monotone slot layout
+  const bool per_seq = rows_max <= bm;
+  const long long slots =
+      per_seq ? sh->num_seqs : static_cast<long long>(sh->total_q) * group / bm + sh->num_seqs;
+  const long long active = per_seq ? std::min<long long>(sh->num_seqs, sh->total_q) : slots;
+  const long long base = std::max<long long>(1, active * hkv);
   // Longest key walk of one q-block: a window bounds it, otherwise the longest sequence.
   long long walk = sh->max_seqlen_k;
   if (window_left >= 0)
     walk = std::min<long long>(walk, static_cast<long long>(window_left) + 1 + (bm + group - 1) / group);
-  const long long target = static_cast<long long>(num_sms) * kTileCtasPerSm;
+  const long long wave = static_cast<long long>(num_sms) * ua::tile_ctas_per_sm(d, kv_dtype, wm);
+  const long long by_walk = std::max<long long>(1, walk / kMinPartitionKeys);
+  const long long fit = std::max<long long>(2, std::min(wave / base, by_walk));
   int n_part = 1;
   if (backend == UA_BACKEND_SPLIT) {
-    if (sh->num_splits > 0) {
-      n_part = sh->num_splits;
-    } else {
-      long long want = std::max<long long>(2, (target + ctas_2d - 1) / std::max<long long>(1, ctas_2d));
-      want = std::min<long long>(want, std::max<long long>(2, (walk + kMinPartitionKeys - 1) / kMinPartitionKeys));
-      n_part = static_cast<int>(want);
-    }
+    n_part = sh->num_splits > 0 ? sh->num_splits : static_cast<int>(fit);
   } else if (backend == UA_BACKEND_AUTO) {
-    if (ctas_2d < target && walk >= 2LL * kMinPartitionKeys) {
-      long long want = (target + ctas_2d - 1) / std::max<long long>(1, ctas_2d);
-      want = std::min<long long>(want, walk / kMinPartitionKeys);
-      n_part = static_cast<int>(std::max<long long>(1, want));
-    }
+    if (base < wave && walk >= 2LL * kMinPartitionKeys) n_part = static_cast<int>(fit);
   }
   n_part = std::min(n_part, kMaxPartitions);
   pl->path = n_part > 1 ? UA_PATH_SPLIT : UA_PATH_2D;
@@ -99,6 +141,17 @@ void make_plan(const ua_shape_t* sh, int hq, int hkv, int d, int window_left, in
   pl->grid_y = hkv;
   pl->grid_z = n_part;
   pl->num_sms = num_sms;
+  // decode-shaped CTAs of one slot read the same cache pages for different kv-heads:
+  // launch them as one cluster so they are scheduled together
+  int cy = 1;
+  if (wm == 1)
+    for (int c = 8; c > 1; c >>= 1)
+      if (hkv % c == 0) {
+        cy = c;
+        break;
+      }
+  pl->cluster_y = cy;
+  pl->slot_per_seq = per_seq ? 1 : 0;
   pl->workspace_bytes = 0;
   if (n_part > 1) {
     const size_t rows = static_cast<size_t>(sh->total_q) * hq * n_part;
@@ -168,10 +221,11 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   int num_sms = 0;
   if ((rc = device_sm_count(&num_sms)) != UA_OK) return rc;
   ua_plan_t pl;
-  make_plan(sh, hq, hkv, d, window_left, backend, num_sms, &pl);
+  make_plan(sh, hq, hkv, d, window_left, kv_dtype, backend, num_sms, &pl);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  ua::AttnParams p{};
+  ua::TileParams tp{};
+  ua::AttnParams& p = tp.p;
   p.q = q;
   p.k = k_cache;
   p.v = v_cache;
@@ -195,6 +249,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   p.qq_stride = sh->qq_bias_stride;
   p.window_left = window_left < 0 ? -1 : window_left;
   p.n_part = pl.n_part;
+  p.slot_per_seq = pl.slot_per_seq;
   p.q_dtype = sh->q_dtype;
   p.out_dtype = sh->out_dtype;
   p.scale = scale;
@@ -219,13 +274,19 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   const int kv = kv_dtype == UA_DT_F16 ? ua::KV_F16 : kv_dtype == UA_DT_BF16 ? ua::KV_BF16 : ua::KV_E4M3;
   const bool feat = softcap > 0.f || alibi != nullptr || qq_bias != nullptr;
   const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
+  // Page-sized TMA boxes need 16 | block_size and row coordinates that fit in int32.
+  bool tma = block_size % 16 == 0 &&
+             static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
+  if (tma)
+    tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
+          encode_cache_map(&tp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d);
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(sh->events);
   if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return UA_ERR_CUDA;
   cudaError_t err;
   switch (d) {
-    case 64: err = ua::launch_tile_d64(p, grid, pl.kernel, kv, feat, st); break;
-    case 128: err = ua::launch_tile_d128(p, grid, pl.kernel, kv, feat, st); break;
-    default: err = ua::launch_tile_d256(p, grid, pl.kernel, kv, feat, st); break;
+    case 64: err = ua::launch_tile_d64(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
+    case 128: err = ua::launch_tile_d128(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
+    default: err = ua::launch_tile_d256(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
   }
   if (err != cudaSuccess) return UA_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], st) != cudaSuccess) return UA_ERR_CUDA;
@@ -273,7 +334,8 @@ int ua_plan(const ua_shape_t* shape, int block_size, int num_q_heads, int num_kv
     int rc = check_sizes(shape, block_size, num_q_heads, num_kv_heads, head_dim, kv_dtype, backend);
     if (rc != UA_OK) return rc;
     if (num_sms <= 0 && (rc = device_sm_count(&num_sms)) != UA_OK) return rc;
-    make_plan(shape, num_q_heads, num_kv_heads, head_dim, window_left, backend, num_sms, plan);
+    make_plan(shape, num_q_heads, num_kv_heads, head_dim, window_left, kv_dtype, backend, num_sms,
+              plan);
     return UA_OK;
   } catch (...) {
     return UA_ERR_CUDA;
@@ -296,7 +358,7 @@ int ua_device_status(void* stream, int* status) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return UA_ERR_CUDA;
   unsigned int word = 0;
   if (cudaMemcpyFromSymbol(&word, g_device_status, sizeof(word)) != cudaSuccess) return UA_ERR_CUDA;
-  *status = (word & ua::DEV_BAD_BLOCK) ? UA_ERR_DEVICE_CHECK
+  *status = (word & (ua::DEV_BAD_BLOCK | ua::DEV_BAD_SHAPE)) ? UA_ERR_DEVICE_CHECK
             : (word & ua::DEV_TIMEOUT) ? UA_ERR_TIMEOUT
                                        : UA_OK;
   return UA_OK;

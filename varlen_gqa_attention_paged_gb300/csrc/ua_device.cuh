@@ -1,9 +1,12 @@
 // ua_device.cuh -- inline-PTX building blocks for the sm_103a kernels of libua.so:
-// mbarriers with bounded waits, bulk async copies (TMA engine, non-tensor form),
+// mbarriers with bounded waits, bulk async copies, programmatic dependent launch,
 // warp-level tensor-core MMA, ldmatrix and fast exp2.
 #pragma once
 
 #include <cstdint>
+#include <utility>
+
+#include <cuda_runtime.h>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -100,6 +103,47 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- dependent launch
+
+// Wait until the grids this one depends on (programmatic stream serialisation) have
+// completed and their memory is visible; a no-op without such a dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid on the stream to be scheduled before this one completes.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialisation (the kernel must call
+// grid_dependency_wait() before it touches memory the previous kernel writes), and,
+// with cluster_y > 1, as clusters of cluster_y CTAs along grid y that the hardware
+// schedules together.
+template <typename... Args, typename... Act>
+inline cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, int cluster_y, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_y > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = static_cast<unsigned>(cluster_y);
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Act>(args)...);
 }
 
 // ---------------------------------------------------------------- warp MMA (m16n8k16)

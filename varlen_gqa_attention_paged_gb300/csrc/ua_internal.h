@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace ua {
@@ -11,7 +12,7 @@ namespace ua {
 enum KvKind { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
 
 // Bits of the device status word (OR-ed by kernels, read by ua_device_status).
-enum : unsigned { DEV_BAD_BLOCK = 1u, DEV_TIMEOUT = 2u };
+enum : unsigned { DEV_BAD_BLOCK = 1u, DEV_TIMEOUT = 2u, DEV_BAD_SHAPE = 4u };
 
 // Everything one launch of the attention tile kernel needs (passed by value).
 struct AttnParams {
@@ -33,8 +34,18 @@ struct AttnParams {
   int num_seqs, total_q, max_seqlen_q, max_blocks_per_seq, num_blocks, block_size;
   int hq, hkv, group;
   int qq_stride, window_left, n_part;
+  int slot_per_seq;             // 1: grid slot x is sequence x (every sequence fits one q-block)
   int q_dtype, out_dtype;
   float scale, softcap;
+};
+
+// Tile-kernel launch argument: the attention parameters plus the TMA tensor maps of the
+// K and V caches, each viewed as a 3-D tensor [num_blocks * block_size][H_kv][D]
+// (used when block_size % 16 == 0; boxes of 16 cache rows x one column block).
+struct TileParams {
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  AttnParams p;
 };
 
 // The LSE-merge of split partitions (one output row per query token x head).
@@ -52,12 +63,15 @@ struct MergeParams {
 // Rows (query token x head of one kv group) per CTA of the tile kernel.
 constexpr int tile_block_m(int wm) { return 16 * wm; }
 
-cudaError_t launch_tile_d64(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
-                            cudaStream_t s);
-cudaError_t launch_tile_d128(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
-                             cudaStream_t s);
-cudaError_t launch_tile_d256(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
-                             cudaStream_t s);
+cudaError_t launch_tile_d64(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
+                            int cluster_y, cudaStream_t s);
+cudaError_t launch_tile_d128(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
+                             int cluster_y, cudaStream_t s);
+cudaError_t launch_tile_d256(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
+                             int cluster_y, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+
+// Resident CTAs per SM of the tile kernel variant for (head_dim, kv dtype, wm).
+int tile_ctas_per_sm(int head_dim, int kv, int wm);
 
 }  // namespace ua

@@ -17,6 +17,8 @@ namespace ua {
 template <int D>
 __global__ void __launch_bounds__(256) ua_merge_kernel(const __grid_constant__ MergeParams p) {
   constexpr int kPer = D / 32;  // output elements per lane
+  grid_dependency_wait();        // the partition kernel's scratch is complete
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
@@ -69,12 +71,11 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
   const dim3 grid((p.rows + 7) / 8);
   switch (p.head_dim) {
-    case 64: ua_merge_kernel<64><<<grid, 256, 0, s>>>(p); break;
-    case 128: ua_merge_kernel<128><<<grid, 256, 0, s>>>(p); break;
-    case 256: ua_merge_kernel<256><<<grid, 256, 0, s>>>(p); break;
+    case 64: return launch_pdl(ua_merge_kernel<64>, grid, dim3(256), 0, s, 1, p);
+    case 128: return launch_pdl(ua_merge_kernel<128>, grid, dim3(256), 0, s, 1, p);
+    case 256: return launch_pdl(ua_merge_kernel<256>, grid, dim3(256), 0, s, 1, p);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace ua

@@ -9,9 +9,13 @@
 // unnormalised output for the merge kernel (the split-KV path of the aiter PR #3962).
 //
 // Warp roles (160 threads):
-//   warp 4      producer: for each tile of T keys it looks every key up in the block
-//               table and issues one bulk async copy (TMA engine) per K row and per V
-//               row into a STAGES-deep shared-memory ring, completing on an mbarrier.
+//   warp 4      producer: gathers each tile of T keys through the block table into a
+//               STAGES-deep shared-memory ring.  With block_size % 16 == 0 every
+//               16-key page slice is one TMA tensor box per column block (completion
+//               counted in bytes on an mbarrier); otherwise 16-byte cp.async copies.
+//               Rows of 128 bytes or more land in the 128-byte swizzled layout (16-byte
+//               chunk c of row r stored at chunk c ^ (r & 7)), which keeps the ldmatrix
+//               reads below free of bank conflicts.
 //   warps 0..3  consumers: QK^T and P.V on tensor cores (mma.sync m16n8k16, fp32
 //               accumulate), score transform, online softmax in base 2 with quad
 //               shuffles, fp8 e4m3 -> f16 dequant of the tile in shared memory.
@@ -22,6 +26,8 @@
 
 #include <atomic>
 #include <climits>
+
+#include <cuda.h>
 
 #include "ua_device.cuh"
 #include "ua_internal.h"
@@ -48,25 +54,48 @@ struct KvTraits<KV_E4M3> {
   static constexpr bool kF16Mma = true;
 };
 
+// Byte offset of 16-byte chunk `c` of row `r` inside a 128-byte-swizzled column block.
+__host__ __device__ constexpr uint32_t sw128(uint32_t r, uint32_t c) {
+  return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
 template <int D, int KV, int WM>
 struct TileCfg {
   static constexpr int kConsumerWarps = 4;
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);
   static constexpr int kWN = kConsumerWarps / WM;  // warps sharing one 16-row m-tile
-  static constexpr int kT = 64;                    // keys per pipeline stage
+  static constexpr int kT = 64;                    // keys per pipeline stage (4 pages of 16)
   static constexpr int kEsz = KvTraits<KV>::kEsz;
   static constexpr int kRowBytes = D * kEsz;       // one K or V row in the cache
-  static constexpr int kRawStride = kRowBytes + 16;     // padded: ldmatrix rows hit 8 bank groups
-  static constexpr int kF16Stride = D * 2 + 16;
-  static constexpr int kStageBytes = 2 * kT * kRawStride;  // K rows then V rows
-  static constexpr int kConvBytes = (KV == KV_E4M3) ? kConsumerWarps * 2 * 16 * kF16Stride : 0;
+  // Rows of 128 bytes or more are stored as 128-byte swizzled column blocks; 64-byte
+  // rows (fp8 with head_dim 64) are stored plainly (only the dequant pass reads them).
+  static constexpr bool kSwz = kRowBytes >= 128;
+  static constexpr int kCBW = kSwz ? 128 : kRowBytes;  // bytes of a row in one column block
+  static constexpr int kCB = kRowBytes / kCBW;         // column blocks per row
+  static constexpr int kCBBytes = kT * kCBW;           // one column block of a tile
+  static constexpr int kStageBytes = 2 * kCB * kCBBytes;  // K then V
+  static constexpr int kConvCB = 16 * 128;                 // f16 column block of 16 rows
+  static constexpr int kConvWarpBytes = 2 * (D / 64) * kConvCB;  // K16 + V16 of one chunk
+  static constexpr int kConvBytes = (KV == KV_E4M3) ? kConsumerWarps * kConvWarpBytes : 0;
   static constexpr int kMergeBytes = (kWN > 1) ? kConsumerWarps * 16 * (D + 2) * 4 : 0;
-  static constexpr int kStages = (4 * kStageBytes + kConvBytes <= 200 * 1024) ? 4 : 3;
-  static constexpr int kPipeBytes =
+  // decode-shaped CTAs aim at two per SM (about 110 KB each); the 64-row variant at one
+  static constexpr int kBudget = (WM == 1 ? 110 : 200) * 1024;
+  static constexpr int kStagesFit = (kBudget - kConvBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit < 2 ? 2 : (kStagesFit > 4 ? 4 : kStagesFit);
+  static constexpr int kPipeRaw =
       (kStages * kStageBytes > kMergeBytes) ? kStages * kStageBytes : kMergeBytes;
-  static constexpr int kSmemBytes = kPipeBytes + kConvBytes + 2 * kStages * 8;
+  static constexpr int kPipeBytes = (kPipeRaw + 1023) & ~1023;
+  static constexpr int kSmemBytes = 1024 + kPipeBytes + kConvBytes + 2 * kStages * 8;
+  static constexpr int kMinBlocks = (2 * kSmemBytes <= 227 * 1024) ? 2 : 1;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kRowBytes % 16 == 0, "bulk copies move 16-byte multiples");
+  static_assert(kRowBytes % kCBW == 0 && kCBW % 16 == 0, "rows are whole column blocks");
+  static_assert(kSwz || KV == KV_E4M3, "16-bit rows are at least 128 bytes");
+
+  // Byte offset of 16-byte chunk c of tile row r in a K or V stage.
+  static __device__ __forceinline__ uint32_t raw_off(uint32_t r, uint32_t c) {
+    if constexpr (kSwz) return (c / 8) * kCBBytes + sw128(r, c % 8);
+    else return r * kCBW + c * 16;
+  }
 };
 
 // Sequence owning q-block slot x: the last b with floor(cu[b] * G / BM) + b <= x
@@ -76,22 +105,52 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int num_
   int lo = 0, hi = num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    const int start = static_cast<int>((static_cast<long long>(__ldg(cu + mid)) * group) / bm) + mid;
+    const int start =
+        static_cast<int>((static_cast<long long>(__ldg(cu + mid)) * group) / bm) + mid;
     if (start <= x) lo = mid;
     else hi = mid - 1;
   }
   return lo;
 }
 
-template <int D, int KV, int WM, bool FEAT>
-__global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_constant__ AttnParams p) {
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
+// The mbarrier receives one arrival once this thread's earlier cp.async copies land.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+template <int D, int KV, int WM, bool FEAT, bool TMA>
+__global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
+    ua_attn_tile_kernel(const __grid_constant__ TileParams tp) {
   using C = TileCfg<D, KV, WM>;
   constexpr int T = C::kT;
   constexpr int S = C::kStages;
   constexpr bool kF16Mma = KvTraits<KV>::kF16Mma;
   constexpr int BM = 16 * WM;
+  const AttnParams& p = tp.p;
+  // Programmatic dependent launch: this grid may be scheduled while the previous kernel
+  // on the stream finishes; it reads nothing before that kernel has completed, and lets
+  // the next kernel (the merge) be scheduled early in turn.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* const smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* const pipe = smem;
   uint8_t* const conv = smem + C::kPipeBytes;
   uint64_t* const full = reinterpret_cast<uint64_t*>(conv + C::kConvBytes);
@@ -104,21 +163,28 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
   const int z = blockIdx.z;
   const int G = p.group;
 
-  // ---- which rows and keys this CTA owns
-  const int b = find_seq(p.cu_seqlens_q, p.num_seqs, blockIdx.x, G, BM);
+  // ---- which rows and keys this CTA owns.  Slot x is sequence x when every sequence
+  // fits one q-block (decode batches: no search); otherwise a binary search over
+  // cu_seqlens_q finds the sequence.
+  const int b = p.slot_per_seq ? static_cast<int>(blockIdx.x)
+                               : find_seq(p.cu_seqlens_q, p.num_seqs, blockIdx.x, G, BM);
   const int q0 = __ldg(p.cu_seqlens_q + b);
   const int q_len = __ldg(p.cu_seqlens_q + b + 1) - q0;
+  const int kv_len = __ldg(p.seq_lens_k + b);
   const int rows_b = q_len * G;
-  const int slot0 = static_cast<int>((static_cast<long long>(q0) * G) / BM) + b;
+  const int slot0 =
+      p.slot_per_seq ? b : static_cast<int>((static_cast<long long>(q0) * G) / BM) + b;
   const int r0 = (static_cast<int>(blockIdx.x) - slot0) * BM;
+  if (p.slot_per_seq && rows_b > BM && threadIdx.x == 0 && z == 0 && g == 0)
+    atomicOr(p.status, DEV_BAD_SHAPE);  // q_len above max_seqlen_q: rows past BM unwritten
   if (r0 < 0 || r0 >= rows_b) return;  // idle slot: uniform for the CTA
   const int r1 = min(r0 + BM, rows_b);
-  const int kv_len = __ldg(p.seq_lens_k + b);
   const int ctx = kv_len - q_len;
   const int pos_first = ctx + r0 / G;
   const int pos_last = ctx + (r1 - 1) / G;
   const int hi = max(0, min(pos_last + 1, kv_len));
-  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0);
+  // the walk starts on a 16-key page boundary; keys before a row's window are masked
+  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
   int part = (hi - lo + p.n_part - 1) / p.n_part;
   part = (part + 15) & ~15;
   const int ks = min(lo + z * part, hi);
@@ -138,62 +204,91 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
   if (warp == C::kConsumerWarps) {
     // ======================================================== producer warp
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-    const size_t slot_pitch = static_cast<size_t>(p.hkv) * C::kRowBytes;
-    const uint8_t* kg = static_cast<const uint8_t*>(p.k) + static_cast<size_t>(g) * C::kRowBytes;
-    const uint8_t* vg = static_cast<const uint8_t*>(p.v) + static_cast<size_t>(g) * C::kRowBytes;
     const uint64_t policy = l2_policy_evict_first();
+    const int bs = p.block_size;
     int issued = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t % S;
-      if (t >= S && !mbar_wait_bounded(&empty[s], ((t / S) & 1) ^ 1, p.status, DEV_TIMEOUT)) break;
-      const int key0 = ks + t * T;
-      const int nvalid = min(T, ke - key0);
-      uint8_t* kdst = pipe + s * C::kStageBytes;
-      uint8_t* vdst = kdst + T * C::kRawStride;
-      size_t off[T / 32];
-      bool ok[T / 32];
-      int bytes = 0;
+    if constexpr (TMA) {
+      // lane j < T/16 owns page slice j (keys key0 + 16j .. +15) of every tile
+      const int oob = p.num_blocks * bs;  // first row coordinate past the cache: zero fill
+      auto page_row = [&](int t) -> int {
+        const int key = ks + t * T + 16 * lane;
+        if (lane >= T / 16 || key >= ke) return oob;
+        const int col = key / bs;
+        const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+          atomicOr(p.status, DEV_BAD_BLOCK);
+          return oob;
+        }
+        return blk * bs + key % bs;
+      };
+      int row_next = ntiles > 0 ? page_row(0) : oob;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % S;
+        const int row = row_next;
+        if (t + 1 < ntiles) row_next = page_row(t + 1);  // block-table lookups one tile ahead
+        if (t >= S &&
+            !mbar_wait_bounded(&empty[s], ((t / S) & 1) ^ 1, p.status, DEV_TIMEOUT))
+          break;
+        uint8_t* kdst = pipe + s * C::kStageBytes;
+        uint8_t* vdst = kdst + C::kCB * C::kCBBytes;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        __syncwarp();
+        if (lane < T / 16) {
 #pragma unroll
-      for (int rr = 0; rr < T / 32; ++rr) {
-        const int row = lane + 32 * rr;
-        ok[rr] = false;
-        off[rr] = 0;
-        if (row < nvalid) {
-          const int key = key0 + row;
-          const int col = key / p.block_size;
-          const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
-          if (static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks)) {
-            ok[rr] = true;
-            off[rr] = (static_cast<size_t>(blk) * p.block_size + key % p.block_size) * slot_pitch;
-            bytes += 2 * C::kRowBytes;
-          } else {
-            atomicOr(p.status, DEV_BAD_BLOCK);
+          for (int cb = 0; cb < C::kCB; ++cb) {
+            const int x = cb * (C::kCBW / C::kEsz);
+            tma_load_3d(kdst + cb * C::kCBBytes + lane * 16 * C::kCBW, &tp.tmap_k, x, g, row,
+                        &full[s], policy);
+            tma_load_3d(vdst + cb * C::kCBBytes + lane * 16 * C::kCBW, &tp.tmap_v, x, g, row,
+                        &full[s], policy);
           }
         }
-        if (!ok[rr]) {  // rows with no key behind them read as zero
-          uint4* kz = reinterpret_cast<uint4*>(kdst + row * C::kRawStride);
-          uint4* vz = reinterpret_cast<uint4*>(vdst + row * C::kRawStride);
-#pragma unroll
-          for (int c = 0; c < C::kRowBytes / 16; ++c) {
-            kz[c] = make_uint4(0, 0, 0, 0);
-            vz[c] = make_uint4(0, 0, 0, 0);
-          }
-        }
+        issued = t + 1;
       }
-      bytes = __reduce_add_sync(0xffffffffu, bytes);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(bytes));
-      __syncwarp();
-#pragma unroll
-      for (int rr = 0; rr < T / 32; ++rr) {
-        if (ok[rr]) {
+    } else {
+      // any block size: 16-byte cp.async per chunk, rows with no key zero-filled
+      const size_t slot_pitch = static_cast<size_t>(p.hkv) * C::kRowBytes;
+      const uint8_t* kg = static_cast<const uint8_t*>(p.k) + static_cast<size_t>(g) * C::kRowBytes;
+      const uint8_t* vg = static_cast<const uint8_t*>(p.v) + static_cast<size_t>(g) * C::kRowBytes;
+      constexpr int kChunks = C::kRowBytes / 16;  // per row
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % S;
+        if (t >= S &&
+            !mbar_wait_bounded(&empty[s], ((t / S) & 1) ^ 1, p.status, DEV_TIMEOUT))
+          break;
+        const int key0 = ks + t * T;
+        uint8_t* kdst = pipe + s * C::kStageBytes;
+        uint8_t* vdst = kdst + C::kCB * C::kCBBytes;
+#pragma unroll 1
+        for (int rr = 0; rr < T / 32; ++rr) {
           const int row = lane + 32 * rr;
-          bulk_copy_g2s(kdst + row * C::kRawStride, kg + off[rr], C::kRowBytes, &full[s], policy);
-          bulk_copy_g2s(vdst + row * C::kRawStride, vg + off[rr], C::kRowBytes, &full[s], policy);
+          const int key = key0 + row;
+          long long off = -1;
+          if (key < ke && key < kv_len) {
+            const int col = key / bs;
+            const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+            if (static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks))
+              off = static_cast<long long>((static_cast<size_t>(blk) * bs + key % bs) * slot_pitch);
+            else
+              atomicOr(p.status, DEV_BAD_BLOCK);
+          }
+#pragma unroll 4
+          for (int c = 0; c < kChunks; ++c) {
+            const uint32_t so = C::raw_off(row, c);
+            if (off >= 0) {
+              cp_async_16(kdst + so, kg + off + 16 * c);
+              cp_async_16(vdst + so, vg + off + 16 * c);
+            } else {
+              *reinterpret_cast<uint4*>(kdst + so) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vdst + so) = make_uint4(0, 0, 0, 0);
+            }
+          }
         }
+        cp_async_arrive(&full[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        issued = t + 1;
       }
-      issued = t + 1;
     }
     // Never leave copies in flight into this CTA's shared memory.
     for (int t = max(0, issued - S); t < issued; ++t)
@@ -294,8 +389,11 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
 #pragma unroll
     for (int e = 0; e < 4; ++e) o_acc[nd][e] = 0.f;
 
-  uint8_t* const conv_k = conv + warp * 2 * 16 * C::kF16Stride;
-  uint8_t* const conv_v = conv_k + 16 * C::kF16Stride;
+  uint8_t* const conv_k = conv + warp * C::kConvWarpBytes;
+  uint8_t* const conv_v = conv_k + (D / 64) * C::kConvCB;
+  // Cache slots at or past kv_len in the sequence's last page hold no key and may hold
+  // anything (NaN included): their P is 0, and their V values are zeroed before P.V so
+  // that 0 * NaN never enters the accumulator.
   bool aborted = false;
 
   for (int t = 0; t < ntiles; ++t) {
@@ -305,28 +403,30 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
       break;
     }
     const uint8_t* kst = pipe + s * C::kStageBytes;
-    const uint8_t* vst = kst + T * C::kRawStride;
+    const uint8_t* vst = kst + C::kCB * C::kCBBytes;
     const int key_tile = ks + t * T;
 
 #pragma unroll 1
-    for (int ch = (WM == 1 ? kgp : 0); ch < 4; ch += (WM == 1 ? 4 : 1)) {
+    for (int ch = (WM == 1 ? kgp : 0); ch < T / 16; ch += (WM == 1 ? 4 : 1)) {
       const int kc0 = key_tile + 16 * ch;
       if (!tile_any || kc0 >= ke || kc0 > pmax || kc0 + 16 <= lomin) continue;
 
-      uint32_t kbase, vbase;
-      int stride;
+      uint32_t kbase, vbase, cbk;
+      int row0;
       if constexpr (KV == KV_E4M3) {
         // Dequantise the chunk's 16 K rows and 16 V rows to f16 (exact); the scales
-        // are applied to the scores and to the output instead.
+        // are applied to the scores and to the output instead.  V rows past kv_len
+        // become zero here.  Each lane turns 16 codes into two 16-byte f16 chunks.
         __syncwarp();
-#pragma unroll
+#pragma unroll 2
         for (int it = 0; it < (2 * 16 * D / 16) / 32; ++it) {
-          const int idx = it * 32 + lane;                // one 16-code group per lane
-          const int which = idx / (16 * D / 16);         // 0: K, 1: V
-          const int rem = idx % (16 * D / 16);
+          const int idx = it * 32 + lane;
+          const int which = idx / D;  // 0: K, 1: V  (16 rows x D/16 groups each)
+          const int rem = idx % D;
           const int row = rem / (D / 16), grp = rem % (D / 16);
-          const uint8_t* src = (which ? vst : kst) + (16 * ch + row) * C::kRawStride + grp * 16;
-          const uint4 raw = *reinterpret_cast<const uint4*>(src);
+          const int trow = 16 * ch + row;
+          uint4 raw = *reinterpret_cast<const uint4*>((which ? vst : kst) + C::raw_off(trow, grp));
+          if (which && kc0 + row >= kv_len) raw = make_uint4(0, 0, 0, 0);
           const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t h[8];
 #pragma unroll
@@ -334,18 +434,22 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
             h[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] & 0xffffu));
             h[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16));
           }
-          uint8_t* dst = (which ? conv_v : conv_k) + row * C::kF16Stride + grp * 32;
-          reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
-          reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+          uint8_t* dst = (which ? conv_v : conv_k) + (grp / 4) * C::kConvCB;
+          const int c16 = (grp % 4) * 2;
+          *reinterpret_cast<uint4*>(dst + sw128(row, c16)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(dst + sw128(row, c16 + 1)) =
+              make_uint4(h[4], h[5], h[6], h[7]);
         }
         __syncwarp();
         kbase = smem_addr(conv_k);
         vbase = smem_addr(conv_v);
-        stride = C::kF16Stride;
+        cbk = C::kConvCB;
+        row0 = 0;
       } else {
-        kbase = smem_addr(kst + 16 * ch * C::kRawStride);
-        vbase = smem_addr(vst + 16 * ch * C::kRawStride);
-        stride = C::kRawStride;
+        kbase = smem_addr(kst);
+        vbase = smem_addr(vst);
+        cbk = C::kCBBytes;
+        row0 = 16 * ch;
       }
 
       // ---- S = Q K^T for 16 keys (two n8 chunks)
@@ -355,12 +459,13 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[n][e] = 0.f;
       {
-        const uint32_t lane_addr =
-            kbase + ((lane & 7) + ((lane >> 4) << 3)) * stride + (((lane >> 3) & 1) << 4);
+        const uint32_t kr = row0 + (lane & 7) + ((lane >> 4) << 3);
+        const uint32_t half = (lane >> 3) & 1;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t c = (kk & 3) * 2 + half;  // 16-byte chunk within the column block
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(lane_addr + kk * 32, b0, b1, b2, b3);
+          ldsm_x4(kbase + (kk >> 2) * cbk + sw128(kr, c), b0, b1, b2, b3);
           mma_16816<kF16Mma>(sc[0], qf[kk], b0, b1);
           mma_16816<kF16Mma>(sc[1], qf[kk], b2, b3);
         }
@@ -441,12 +546,27 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
         }
       }
       {
-        const uint32_t lane_addr =
-            vbase + ((lane & 7) + (((lane >> 3) & 1) << 3)) * stride + ((lane >> 4) << 4);
+        const uint32_t vr = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const uint32_t dh = lane >> 4;
+        const int k0 = kc0 + 2 * cq;
+        const bool tail = kc0 + 16 > kv_len;
+        // b0/b2 hold keys k0, k0+1 and b1/b3 keys k0+8, k0+9 of the chunk
+        const uint32_t m01 = (k0 < kv_len ? 0xffffu : 0u) | (k0 + 1 < kv_len ? 0xffff0000u : 0u);
+        const uint32_t m89 =
+            (k0 + 8 < kv_len ? 0xffffu : 0u) | (k0 + 9 < kv_len ? 0xffff0000u : 0u);
 #pragma unroll
         for (int nd = 0; nd < D / 8; nd += 2) {
+          const uint32_t c = (nd & 7) + dh;  // 16-byte chunk within the column block
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(lane_addr + nd * 16, b0, b1, b2, b3);
+          ldsm_x4_trans(vbase + (nd >> 3) * cbk + sw128(vr, c), b0, b1, b2, b3);
+          if constexpr (KV != KV_E4M3) {
+            if (tail) {
+              b0 &= m01;
+              b2 &= m01;
+              b1 &= m89;
+              b3 &= m89;
+            }
+          }
           mma_16816<kF16Mma>(o_acc[nd], pa, b0, b1);
           mma_16816<kF16Mma>(o_acc[nd + 1], pa, b2, b3);
           if constexpr (!kF16Mma) {
@@ -578,10 +698,10 @@ __global__ void __launch_bounds__(160, 1) ua_attn_tile_kernel(const __grid_const
   }
 }
 
-template <int D, int KV, int WM, bool FEAT>
-cudaError_t launch_tile_t(const AttnParams& p, dim3 grid, cudaStream_t stream) {
+template <int D, int KV, int WM, bool FEAT, bool TMA>
+cudaError_t launch_tile_t(const TileParams& tp, dim3 grid, int cluster_y, cudaStream_t stream) {
   using C = TileCfg<D, KV, WM>;
-  auto kern = ua_attn_tile_kernel<D, KV, WM, FEAT>;
+  auto kern = ua_attn_tile_kernel<D, KV, WM, FEAT, TMA>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -592,17 +712,20 @@ cudaError_t launch_tile_t(const AttnParams& p, dim3 grid, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     configured.fetch_or(bit);
   }
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, cluster_y, tp);
 }
 
 template <int D>
-cudaError_t launch_tile_dispatch(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
-                                 cudaStream_t s) {
-#define UA_TILE_CASE(KVV, WMV)                                                  \
-  if (kv == KVV && wm == WMV)                                                   \
-    return feat ? launch_tile_t<D, KVV, WMV, true>(p, grid, s)                  \
-                : launch_tile_t<D, KVV, WMV, false>(p, grid, s);
+cudaError_t launch_tile_dispatch(const TileParams& tp, dim3 grid, int wm, int kv, bool feat,
+                                 bool tma, int cluster_y, cudaStream_t s) {
+#define UA_TILE_CASE(KVV, WMV)                                                        \
+  if (kv == KVV && wm == WMV) {                                                       \
+    if (tma)                                                                          \
+      return feat ? launch_tile_t<D, KVV, WMV, true, true>(tp, grid, cluster_y, s)    \
+                  : launch_tile_t<D, KVV, WMV, false, true>(tp, grid, cluster_y, s);  \
+    return feat ? launch_tile_t<D, KVV, WMV, true, false>(tp, grid, cluster_y, s)     \
+                : launch_tile_t<D, KVV, WMV, false, false>(tp, grid, cluster_y, s);   \
+  }
   UA_TILE_CASE(KV_F16, 1)
   UA_TILE_CASE(KV_F16, 4)
   UA_TILE_CASE(KV_BF16, 1)
@@ -611,6 +734,13 @@ cudaError_t launch_tile_dispatch(const AttnParams& p, dim3 grid, int wm, int kv,
   UA_TILE_CASE(KV_E4M3, 4)
 #undef UA_TILE_CASE
   return cudaErrorInvalidValue;
+}
+
+template <int D>
+int tile_ctas_per_sm_d(int kv, int wm) {
+  if (kv == KV_E4M3)
+    return wm == 1 ? TileCfg<D, KV_E4M3, 1>::kMinBlocks : TileCfg<D, KV_E4M3, 4>::kMinBlocks;
+  return wm == 1 ? TileCfg<D, KV_BF16, 1>::kMinBlocks : TileCfg<D, KV_BF16, 4>::kMinBlocks;
 }
 
 }  // namespace ua

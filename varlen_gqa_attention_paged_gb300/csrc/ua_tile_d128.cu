@@ -3,9 +3,15 @@
 
 namespace ua {
 
-cudaError_t launch_tile_d128(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
-                             cudaStream_t s) {
-  return launch_tile_dispatch<128>(p, grid, wm, kv, feat, s);
+cudaError_t launch_tile_d128(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
+                             int cluster_y, cudaStream_t s) {
+  return launch_tile_dispatch<128>(tp, grid, wm, kv, feat, tma, cluster_y, s);
+}
+
+int tile_ctas_per_sm(int head_dim, int kv, int wm) {
+  if (head_dim == 64) return tile_ctas_per_sm_d<64>(kv, wm);
+  if (head_dim == 256) return tile_ctas_per_sm_d<256>(kv, wm);
+  return tile_ctas_per_sm_d<128>(kv, wm);
 }
 
 }  // namespace ua

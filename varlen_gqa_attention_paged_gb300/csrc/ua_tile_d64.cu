@@ -3,9 +3,9 @@
 
 namespace ua {
 
-cudaError_t launch_tile_d64(const AttnParams& p, dim3 grid, int wm, int kv, bool feat,
-                             cudaStream_t s) {
-  return launch_tile_dispatch<64>(p, grid, wm, kv, feat, s);
+cudaError_t launch_tile_d64(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
+                             int cluster_y, cudaStream_t s) {
+  return launch_tile_dispatch<64>(tp, grid, wm, kv, feat, tma, cluster_y, s);
 }
 
 }  // namespace ua
