@@ -141,6 +141,21 @@ class ClockSampler:
                 "samples": len(sel), "window": window}
 
 
+def max_over_ranks(elapsed_ms, world, device):
+    """The slowest rank's timed-region length (replicas: each rank runs its own copy)."""
+    if world <= 1:
+        return float(elapsed_ms)
+    import torch.distributed as dist
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step, steps, elapsed_ms, world):
+    """Whole-job tokens/s: every rank processes its own steps (weak scaling)."""
+    return world * tokens_per_step * steps / (elapsed_ms * 1e-3)
+
+
 # --------------------------------------------------------------------------- our arm
 
 class Call:
@@ -299,11 +314,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     attn_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
     merge_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
 
@@ -360,7 +371,7 @@ def run_ours(args):
     if rank != 0:
         return
     tokens_per_step = inp.total_q
-    value = world * tokens_per_step * args.steps / (elapsed_ms * 1e-3)
+    value = job_throughput(tokens_per_step, args.steps, elapsed_ms, world)
     attn_us = statistics.mean(attn_ms) * 1e3
     kbytes = W.kv_bytes_read(inp)
     achieved = kbytes / (attn_us * 1e-6) / 1e9
