@@ -56,6 +56,9 @@ extern "C" {
 
 #define UA_VERSION 100
 
+/* Size of the fixed device scratch array used by ua_unified_attention_noalloc. */
+#define UA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
 typedef enum {
   UA_OK = 0,
   UA_ERR_INVALID_ARG = 1,  /* a size, pointer, alignment or enum value is not accepted */
@@ -63,7 +66,9 @@ typedef enum {
   UA_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, allocation, query) */
   UA_ERR_WORKSPACE = 4,    /* the caller's workspace is smaller than ua_plan() asks */
   UA_ERR_DEVICE_CHECK = 5, /* a kernel saw a block id outside [0, num_blocks) */
-  UA_ERR_TIMEOUT = 6       /* a kernel gave up waiting on its own copy pipeline */
+  UA_ERR_TIMEOUT = 6,      /* a kernel gave up waiting on its own copy pipeline */
+  UA_ERR_SCRATCH_LIMIT = 7 /* ua_unified_attention_noalloc: the call needs more scratch than
+                              its fixed UA_NOALLOC_SCRATCH_BYTES */
 } ua_status_t;
 
 typedef enum { UA_DT_F16 = 0, UA_DT_BF16 = 1, UA_DT_F8E4M3 = 2, UA_DT_F32 = 3 } ua_dtype_t;
@@ -144,6 +149,39 @@ int ua_unified_attention(const void* q, const void* k_cache, const void* v_cache
                          int window_left, const float* alibi_slopes, const float* qq_bias,
                          const float* sinks, int kv_dtype, const float* kv_scale, int backend,
                          void* stream, const ua_shape_t* shape);
+
+/*
+ * ua_unified_attention_noalloc -- ua_unified_attention for callers that may not
+ * allocate device memory (the pages have no counterpart: this is a library service).
+ *
+ * Some callers cannot call cudaMalloc: a serving runtime that gives all free device
+ * memory to its own cache pool at start-up, a process held to a fixed memory budget,
+ * or a latency-critical loop where an allocation (which can block and synchronise the
+ * device) is not allowed.  ua_unified_attention allocates only when the split-KV path
+ * runs without a caller workspace; this entry point runs the same kernels but keeps the
+ * split path's scratch in one fixed device array of UA_NOALLOC_SCRATCH_BYTES that the
+ * library holds on every GPU that loads it, until the process exits.  It never calls
+ * cudaMalloc or cudaFree.
+ *
+ * Arguments and results are those of ua_unified_attention, except that
+ * shape->workspace is ignored.  Extra behaviour:
+ *   - UA_ERR_SCRATCH_LIMIT, before anything is launched, when the plan needs more than
+ *     UA_NOALLOC_SCRATCH_BYTES of scratch (ua_plan reports workspace_bytes).
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array: calls whose kernels overlap on the
+ *     GPU (different streams, or several host threads) race on it and give wrong
+ *     results.  Calls on one stream are ordered and safe.  The array keeps the last
+ *     call's contents; nothing in it needs to start at zero.
+ */
+int ua_unified_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                 void* out, const int32_t* cu_seqlens_q,
+                                 const int32_t* seq_lens_k, const int32_t* block_table,
+                                 int block_size, int num_q_heads, int num_kv_heads, int head_dim,
+                                 float scale, float softcap, int window_left,
+                                 const float* alibi_slopes, const float* qq_bias,
+                                 const float* sinks, int kv_dtype, const float* kv_scale,
+                                 int backend, void* stream, const ua_shape_t* shape);
 
 /*
  * ua_plan -- the dispatcher's decision for a call with these sizes, without touching

@@ -9,7 +9,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libua.so")
 
 # ua_status_t
 UA_OK, UA_ERR_INVALID_ARG, UA_ERR_UNSUPPORTED, UA_ERR_CUDA = 0, 1, 2, 3
-UA_ERR_WORKSPACE, UA_ERR_DEVICE_CHECK, UA_ERR_TIMEOUT = 4, 5, 6
+UA_ERR_WORKSPACE, UA_ERR_DEVICE_CHECK, UA_ERR_TIMEOUT, UA_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
+UA_NOALLOC_SCRATCH_BYTES = 16 << 20
 # ua_dtype_t
 UA_DT_F16, UA_DT_BF16, UA_DT_F8E4M3, UA_DT_F32 = 0, 1, 2, 3
 # ua_backend_t
@@ -18,7 +19,7 @@ UA_BACKEND_AUTO, UA_BACKEND_2D, UA_BACKEND_SPLIT = 0, 1, 2
 UA_PATH_2D, UA_PATH_SPLIT = 1, 2
 
 # every symbol include/ua.h declares
-EXPORTS = ("ua_unified_attention", "ua_plan", "ua_workspace_bytes", "ua_device_status",
+EXPORTS = ("ua_unified_attention", "ua_unified_attention_noalloc", "ua_plan", "ua_workspace_bytes", "ua_device_status",
            "ua_device_status_reset", "ua_status_string", "ua_version")
 
 
@@ -76,6 +77,8 @@ def load():
                                              f32, i32, vp, vp, vp, i32, vp, i32, vp,
                                              ctypes.POINTER(UaShape)]
         lib.ua_unified_attention.restype = ctypes.c_int
+        lib.ua_unified_attention_noalloc.argtypes = lib.ua_unified_attention.argtypes
+        lib.ua_unified_attention_noalloc.restype = ctypes.c_int
         lib.ua_plan.argtypes = [ctypes.POINTER(UaShape), i32, i32, i32, i32, i32, i32, i32, i32,
                                 ctypes.POINTER(UaPlan)]
         lib.ua_plan.restype = ctypes.c_int

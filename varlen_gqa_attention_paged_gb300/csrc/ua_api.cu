@@ -382,6 +382,8 @@ const char* ua_status_string(int status) {
     case UA_ERR_WORKSPACE: return "workspace too small";
     case UA_ERR_DEVICE_CHECK: return "device check failed: block id outside the cache";
     case UA_ERR_TIMEOUT: return "device wait timed out";
+    case UA_ERR_SCRATCH_LIMIT:
+      return "call needs more scratch than the fixed array of ua_unified_attention_noalloc";
     default: return "unknown status";
   }
 }
