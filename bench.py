@@ -422,6 +422,20 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_launches(args):
+    """warmup + steps calls of the workload on cuda:0, nothing else (for ncu captures)."""
+    spec = W.WORKLOADS[args.workload]
+    inp = W.make(spec, replicas=n_replicas(spec))
+    call = Call(inp, torch.device("cuda", 0), backend=args.backend)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            call(stream, replica=i)
+    torch.cuda.synchronize()
+    print(json.dumps({"launch_only": spec.name, "calls": args.warmup + args.steps,
+                      "plan": call.plan}))
+
+
 def cpu_baseline(inp, budget_s=12.0, sample_seqs=None):
     """The oracle as it stands, on the host cores, over a bounded sample of the workload."""
     import oracle
@@ -502,10 +516,16 @@ def main():
     ap.add_argument("--workload-steps", type=int, default=20)
     ap.add_argument("--skip-workloads", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--launch-only", action="store_true",
+                    help="only run --warmup + --steps calls of --workload (a small, fixed "
+                         "launch sequence for profilers); print nothing else")
+    ap.add_argument("--backend", default="auto", choices=["auto", "2d", "split"])
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.launch_only:
+        run_launches(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
