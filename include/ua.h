@@ -105,8 +105,10 @@ typedef struct {
 /* What the dispatcher chose for a call (see ua_plan). */
 typedef struct {
   int32_t path;        /* ua_path_t */
-  int32_t kernel;      /* 1: tensor-core tile kernel with 16 rows per CTA (decode-shaped
-                          q-blocks), 4: tile kernel with 64 rows per CTA */
+  int32_t kernel;      /* 1: warp-MMA tile kernel, 16 rows per CTA (decode-shaped q-blocks);
+                          4: warp-MMA tile kernel, 64 rows per CTA (fp8 caches, block sizes
+                          not a multiple of 16); 8: tensor-memory (tcgen05) kernel with
+                          128-row q-blocks of floor(128 / G) tokens x G heads */
   int32_t block_m;     /* (query token x head) rows per q-block */
   int32_t n_part;      /* key-range partitions (1 on the 2D path) */
   int32_t grid_x;      /* q-block slots: num_seqs when slot_per_seq, else

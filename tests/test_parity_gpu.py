@@ -103,6 +103,19 @@ SMALL = {
     "window1": dict(window=1, sinks=True),
     "kv_shorter_than_q": dict(seqs=[(4, 2), (1, 0), (6, 6), (2, 40)], sinks=True),
     "g32_decode": dict(seqs=[(1, 700), (1, 33)], num_q_heads=32, num_kv_heads=1),
+    # prefill-shaped blocks on the tensor-memory kernel: several key tiles, the window and
+    # sinks, partial last pages, rows past the last token of a sequence
+    "pf_bf16_window_sinks": dict(seqs=[(200, 500), (129, 129), (1, 300), (37, 45)],
+                                 num_q_heads=32, num_kv_heads=8, q_dtype=torch.bfloat16,
+                                 kv_dtype=torch.bfloat16, window=150, sinks=True),
+    "pf_f16_mha_d64_bs32": dict(seqs=[(150, 333), (20, 20)], num_q_heads=4, num_kv_heads=4,
+                                head_dim=64, block_size=32),
+    "pf_bf16_g16_d256_feat": dict(seqs=[(40, 500), (9, 9)], num_q_heads=16, num_kv_heads=1,
+                                  head_dim=256, block_size=64, q_dtype=torch.bfloat16,
+                                  kv_dtype=torch.bfloat16, softcap=30.0, alibi=True,
+                                  qq_bias=True, qq_bias_shape=(64, 64), sinks=True),
+    "pf_f16_g6_chunk": dict(seqs=[(70, 600), (1, 17)], num_q_heads=12, num_kv_heads=2,
+                            window=300),
 }
 
 

@@ -58,6 +58,26 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// q [total_q][H_q][D] as a 3-D TMA tensor; one box is the 64-element column block `x` of
+// G heads x tq tokens, written as G*tq rows of 128 bytes (128-byte swizzle).
+bool encode_q_map(CUtensorMap* map, const void* q, int q_dtype, int total_q, int hq, int d,
+                  int group, int tq) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hq),
+                              static_cast<cuuint64_t>(total_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(d) * 2 * hq};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tq)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      enc(map, q_dtype == UA_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+          3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // A paged cache [num_blocks * block_size][H_kv][D] as a 3-D TMA tensor; one box is 16
 // cache rows of one kv-head and one column block (128 bytes, swizzled; 64-byte rows
 // unswizzled).  Rows past the tensor read as zero.
@@ -107,23 +127,34 @@ int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, in
 // part of one wave of SMs idle and the walk spans at least two minimum partitions;
 // then into as many partitions as still fit in that one wave (at least two): a
 // second, partly filled wave costs more than the extra parallelism gives back.
-void make_plan(const ua_shape_t* sh, int hq, int hkv, int d, int window_left, int kv_dtype,
-               int backend, int num_sms, ua_plan_t* pl) {
+//
+// Kernel: decode-shaped calls (every sequence's rows fit 16) take the warp-MMA tile kernel
+// with 16-row q-blocks; other calls on fp16/bf16 caches with 16 | block_size take the
+// tensor-memory kernel with 128-row q-blocks (floor(128 / G) tokens x G heads); the rest
+// (fp8 caches, other block sizes) take the tile kernel with 64-row q-blocks.
+void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int window_left,
+               int kv_dtype, int backend, int num_sms, bool allow_tc, ua_plan_t* pl) {
   const int group = hq / hkv;
   const long long rows_max = static_cast<long long>(sh->max_seqlen_q) * group;
+  const bool tc = allow_tc && rows_max > 16 && group <= 128 && block_size % 16 == 0 &&
+                  (kv_dtype == UA_DT_F16 || kv_dtype == UA_DT_BF16);
   const int wm = rows_max <= 16 ? 1 : 4;
-  const int bm = ua::tile_block_m(wm);
+  const int tq = tc ? 128 / group : 0;               // tokens per tensor-memory q-block
+  const int bm = tc ? tq * group : ua::tile_block_m(wm);
   // every sequence fits one q-block: slot x is sequence x; else the monotone slot layout
-  const bool per_seq = rows_max <= bm;
+  const bool per_seq = !tc && rows_max <= bm;
   const long long slots =
-      per_seq ? sh->num_seqs : static_cast<long long>(sh->total_q) * group / bm + sh->num_seqs;
+      tc ? static_cast<long long>(sh->total_q) / tq + sh->num_seqs
+         : per_seq ? sh->num_seqs
+                   : static_cast<long long>(sh->total_q) * group / bm + sh->num_seqs;
   const long long active = per_seq ? std::min<long long>(sh->num_seqs, sh->total_q) : slots;
   const long long base = std::max<long long>(1, active * hkv);
   // Longest key walk of one q-block: a window bounds it, otherwise the longest sequence.
   long long walk = sh->max_seqlen_k;
   if (window_left >= 0)
     walk = std::min<long long>(walk, static_cast<long long>(window_left) + 1 + (bm + group - 1) / group);
-  const long long wave = static_cast<long long>(num_sms) * ua::tile_ctas_per_sm(d, kv_dtype, wm);
+  const long long wave =
+      static_cast<long long>(num_sms) * (tc ? 1 : ua::tile_ctas_per_sm(d, kv_dtype, wm));
   const long long by_walk = std::max<long long>(1, walk / kMinPartitionKeys);
   const long long fit = std::max<long long>(2, std::min(wave / base, by_walk));
   int n_part = 1;
@@ -134,7 +165,7 @@ void make_plan(const ua_shape_t* sh, int hq, int hkv, int d, int window_left, in
   }
   n_part = std::min(n_part, kMaxPartitions);
   pl->path = n_part > 1 ? UA_PATH_SPLIT : UA_PATH_2D;
-  pl->kernel = wm;
+  pl->kernel = tc ? ua::KERNEL_TC128 : wm;
   pl->block_m = bm;
   pl->n_part = n_part;
   pl->grid_x = static_cast<int32_t>(slots);
@@ -144,7 +175,7 @@ void make_plan(const ua_shape_t* sh, int hq, int hkv, int d, int window_left, in
   // decode-shaped CTAs of one slot read the same cache pages for different kv-heads:
   // launch them as one cluster so they are scheduled together
   int cy = 1;
-  if (wm == 1)
+  if (!tc && wm == 1)
     for (int c = 8; c > 1; c >>= 1)
       if (hkv % c == 0) {
         cy = c;
@@ -221,7 +252,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   int num_sms = 0;
   if ((rc = device_sm_count(&num_sms)) != UA_OK) return rc;
   ua_plan_t pl;
-  make_plan(sh, hq, hkv, d, window_left, kv_dtype, backend, num_sms, &pl);
+  make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, true, &pl);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   ua::TileParams tp{};
@@ -257,6 +288,24 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return UA_ERR_CUDA;
 
+  const int kv = kv_dtype == UA_DT_F16 ? ua::KV_F16 : kv_dtype == UA_DT_BF16 ? ua::KV_BF16 : ua::KV_E4M3;
+  const bool feat = softcap > 0.f || alibi != nullptr || qq_bias != nullptr;
+  // The tensor-memory kernel needs TMA maps of q and both caches; if one cannot be made,
+  // the call is planned again for the tile kernel.
+  ua::PrefillParams pp{};
+  if (pl.kernel == ua::KERNEL_TC128) {
+    const int group = hq / hkv;
+    const bool maps =
+        static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX &&
+        encode_q_map(&pp.tmap_q, q, sh->q_dtype, sh->total_q, hq, d, group, 128 / group) &&
+        encode_cache_map(&pp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
+        encode_cache_map(&pp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d);
+    if (!maps) {
+      make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, false, &pl);
+      p.n_part = pl.n_part;
+    }
+    pp.tq = 128 / group;
+  }
   if (pl.n_part > 1) {
     void* ws = sh->workspace;
     if (ws != nullptr) {
@@ -270,12 +319,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
     p.ws_l = reinterpret_cast<float*>(static_cast<char*>(ws) + ml);
     p.ws_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ml);
   }
-
-  const int kv = kv_dtype == UA_DT_F16 ? ua::KV_F16 : kv_dtype == UA_DT_BF16 ? ua::KV_BF16 : ua::KV_E4M3;
-  const bool feat = softcap > 0.f || alibi != nullptr || qq_bias != nullptr;
   const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
   // Page-sized TMA boxes need 16 | block_size and row coordinates that fit in int32.
-  bool tma = block_size % 16 == 0 &&
+  bool tma = pl.kernel != ua::KERNEL_TC128 && block_size % 16 == 0 &&
              static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
   if (tma)
     tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
@@ -283,7 +329,14 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(sh->events);
   if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return UA_ERR_CUDA;
   cudaError_t err;
-  switch (d) {
+  if (pl.kernel == ua::KERNEL_TC128) {
+    pp.p = p;
+    switch (d) {
+      case 64: err = ua::launch_prefill_d64(pp, grid, kv, feat, st); break;
+      case 128: err = ua::launch_prefill_d128(pp, grid, kv, feat, st); break;
+      default: err = ua::launch_prefill_d256(pp, grid, kv, feat, st); break;
+    }
+  } else switch (d) {
     case 64: err = ua::launch_tile_d64(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
     case 128: err = ua::launch_tile_d128(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
     default: err = ua::launch_tile_d256(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
@@ -334,8 +387,8 @@ int ua_plan(const ua_shape_t* shape, int block_size, int num_q_heads, int num_kv
     int rc = check_sizes(shape, block_size, num_q_heads, num_kv_heads, head_dim, kv_dtype, backend);
     if (rc != UA_OK) return rc;
     if (num_sms <= 0 && (rc = device_sm_count(&num_sms)) != UA_OK) return rc;
-    make_plan(shape, num_q_heads, num_kv_heads, head_dim, window_left, kv_dtype, backend, num_sms,
-              plan);
+    make_plan(shape, block_size, num_q_heads, num_kv_heads, head_dim, window_left, kv_dtype,
+              backend, num_sms, true, plan);
     return UA_OK;
   } catch (...) {
     return UA_ERR_CUDA;

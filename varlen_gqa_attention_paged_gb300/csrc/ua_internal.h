@@ -48,6 +48,17 @@ struct TileParams {
   AttnParams p;
 };
 
+// Tensor-memory prefill kernel launch argument: tensor maps of q viewed as
+// [total_q][H_q][D] (box: 64 elements x G heads x tq tokens) and of the two caches, the
+// attention parameters, and tq = query tokens per 128-row q-block (floor(128 / G)).
+struct PrefillParams {
+  CUtensorMap tmap_q;
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  AttnParams p;
+  int tq;
+};
+
 // The LSE-merge of split partitions (one output row per query token x head).
 struct MergeParams {
   const float* ws_m;
@@ -70,6 +81,12 @@ cudaError_t launch_tile_d128(const TileParams& tp, dim3 grid, int wm, int kv, bo
 cudaError_t launch_tile_d256(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
                              int cluster_y, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+cudaError_t launch_prefill_d64(const PrefillParams& pp, dim3 grid, int kv, bool feat, cudaStream_t s);
+cudaError_t launch_prefill_d128(const PrefillParams& pp, dim3 grid, int kv, bool feat, cudaStream_t s);
+cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool feat, cudaStream_t s);
+
+// Plan kernel codes.
+enum : int { KERNEL_TILE16 = 1, KERNEL_TILE64 = 4, KERNEL_TC128 = 8 };
 
 // Resident CTAs per SM of the tile kernel variant for (head_dim, kv dtype, wm).
 int tile_ctas_per_sm(int head_dim, int kv, int wm);

@@ -1,0 +1,517 @@
+// ua_prefill.cuh -- the tensor-memory attention kernel of libua.so for prefill-shaped
+// q-blocks (included by ua_prefill_d*.cu).
+//
+// One CTA owns (q-block, kv-head g, key partition z).  A q-block is TQ consecutive query
+// tokens of one sequence times the G query heads that read kv-head g, packed as
+// M = 128 rows of a 5th-generation tensor-core tile (row r = token r / G, head r % G;
+// TQ = floor(128 / G)), so the GQA heads of a group share every K/V tile (vllm-rdna PR
+// #34 "FA-RDNA2 D=128 prefill", "Change" 1, on tensor cores).  Per key tile of BN keys:
+//
+//   S = Q K^T    tcgen05.mma (kind::f16, M=128, N=BN, fp32 accumulate) into tensor memory
+//   softmax      one thread per row reads its S row from tensor memory, applies scale,
+//                softcap, ALiBi, QQ-bias and the causal/window mask, updates the running
+//                max and sum in base 2 (the sink is the initial max), and writes
+//                P = 2^(s - m) to shared memory as bf16 (high part + remainder) or f16
+//   O += P V     tcgen05.mma into tensor memory (V is the MN-major operand as it lands)
+//
+// S is double-buffered in tensor memory, so the MMA warp computes S of tile j+1 while the
+// softmax warps work on tile j.  O is rescaled only when a row's max grows by more than
+// 2^8 (the sum and O stay consistent with the max actually used), which keeps tensor
+// memory round trips rare.
+//
+// Warp roles (192 threads):  warps 0..3 softmax + epilogue (thread = row = TMEM lane),
+// warp 4 TMA producer (Q once, then K/V pages of 16 keys through the block table into a
+// 2-stage ring, 128-byte swizzled), warp 5 MMA issuer and tensor-memory owner.
+#pragma once
+
+#include <atomic>
+#include <climits>
+
+#include <cuda.h>
+
+#include "ua_device.cuh"
+#include "ua_internal.h"
+
+#include "ua.h"
+
+namespace ua {
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int kBM = 128;                        // MMA rows
+  static constexpr int kBN = D >= 256 ? 64 : 128;        // keys per tile
+  static constexpr int kCB = D / 64;                     // 128-byte column blocks of a row
+  static constexpr int kQBytes = kCB * kBM * 128;
+  static constexpr int kKVCB = kBN * 128;                // one column block of a K or V tile
+  static constexpr int kStageBytes = 2 * kCB * kKVCB;    // K then V
+  static constexpr int kStages = 2;
+  static constexpr int kPCB = kBM * 128;                 // one column block (64 keys) of P
+  static constexpr int kPBytes = (kBN / 64) * kPCB;
+  static constexpr int kSmemBytes =
+      1024 + kQBytes + kStages * kStageBytes + 2 * kPBytes + 256;
+  static constexpr int kTmemCols = 512;                  // S0, S1, O  (2*BN + D <= 512)
+  static constexpr int kThreads = 192;
+  static_assert(2 * kBN + D <= kTmemCols, "tensor memory budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void tma_load_3d_pf(void* dst, const CUtensorMap* map, int x, int y,
+                                               int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bounded wait that also gives up at once when another warp of the CTA already did.
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        unsigned int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, DEV_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Sequence owning token-block slot x: the last b with floor(cu[b] / TQ) + b <= x.
+__device__ __forceinline__ int pf_find_seq(const int32_t* __restrict__ cu, int num_seqs, int x,
+                                           int tq) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) / tq + mid <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int D, bool BF16, bool FEAT>
+__global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_constant__ PrefillParams pp) {
+  using C = PrefillCfg<D>;
+  constexpr int BN = C::kBN;
+  const AttnParams& p = pp.p;
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* const smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* const sQ = smem;
+  uint8_t* const sKV = sQ + C::kQBytes;
+  uint8_t* const sP = sKV + C::kStages * C::kStageBytes;  // P high part, then P low part
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(sP + 2 * C::kPBytes);
+  uint64_t* const q_full = bars + 0;
+  uint64_t* const kv_full = bars + 1;   // [2]
+  uint64_t* const kv_empty = bars + 3;  // [2]
+  uint64_t* const s_full = bars + 5;    // [2]
+  uint64_t* const s_free = bars + 7;    // [2]
+  uint64_t* const p_full = bars + 9;
+  uint64_t* const pv_done = bars + 10;
+  uint64_t* const fin = bars + 11;
+  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(bars + 12);
+  int* const lo_flag = reinterpret_cast<int*>(bars + 13);  // [2]: tile index + 1 when the
+                                                            // low part of P matters
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.y;
+  const int z = blockIdx.z;
+  const int G = p.group;
+  const int TQ = pp.tq;
+
+  // Longest walks first: slots are taken in reverse order.
+  const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  const int b = pf_find_seq(p.cu_seqlens_q, p.num_seqs, x, TQ);
+  const int q0 = __ldg(p.cu_seqlens_q + b);
+  const int q_len = __ldg(p.cu_seqlens_q + b + 1) - q0;
+  const int kv_len = __ldg(p.seq_lens_k + b);
+  const int t_first = (x - (q0 / TQ + b)) * TQ;  // first token of the block within the sequence
+  if (t_first < 0 || t_first >= q_len) return;   // idle slot: uniform for the CTA
+  const int t_last = min(t_first + TQ, q_len) - 1;
+  const int rows = (t_last - t_first + 1) * G;   // valid rows of the 128
+  const int ctx = kv_len - q_len;
+  const int pos_first = ctx + t_first, pos_last = ctx + t_last;
+  const int hi = max(0, min(pos_last + 1, kv_len));
+  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
+  int part = (hi - lo + p.n_part - 1) / p.n_part;
+  part = (part + 15) & ~15;
+  const int ks = min(lo + z * part, hi);
+  const int ke = min(ks + part, hi);
+  const int nt = (ke - ks + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      lo_flag[i] = 0;
+    }
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(fin, 1);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  // Q rows past the block stay zero (they are computed and dropped).
+  for (int i = threadIdx.x; i < C::kCB * (C::kBM - TQ * G) * 8; i += C::kThreads) {
+    const int cb = i / ((C::kBM - TQ * G) * 8), rem = i % ((C::kBM - TQ * G) * 8);
+    *reinterpret_cast<uint4*>(sQ + cb * C::kBM * 128 + (TQ * G + rem / 8) * 128 + (rem % 8) * 16) =
+        make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS[2] = {tmem, tmem + BN};
+  const uint32_t tO = tmem + 2 * BN;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 4) {
+    // ======================================================== TMA producer
+    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    const int bs = p.block_size;
+    const int oob = p.num_blocks * bs;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, C::kCB * TQ * G * 128);
+      for (int cb = 0; cb < C::kCB; ++cb)
+        tma_load_3d_pf(sQ + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G, q0 + t_first, q_full);
+    }
+    auto page_row = [&](int j) -> int {
+      const int key = ks + j * BN + 16 * lane;
+      if (lane >= BN / 16 || key >= ke) return oob;
+      const int col = key / bs;
+      const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+      if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+        atomicOr(p.status, DEV_BAD_BLOCK);
+        return oob;
+      }
+      return blk * bs + key % bs;
+    };
+    int row_next = nt > 0 ? page_row(0) : oob;
+    int issued = 0;
+    for (int j = 0; j < nt; ++j) {
+      const int s = j & 1;
+      const int row = row_next;
+      if (j + 1 < nt) row_next = page_row(j + 1);
+      if (j >= 2 && !pf_wait(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.status)) break;
+      uint8_t* kd = sKV + s * C::kStageBytes;
+      uint8_t* vd = kd + C::kCB * C::kKVCB;
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
+      __syncwarp();
+      if (lane < BN / 16) {
+#pragma unroll
+        for (int cb = 0; cb < C::kCB; ++cb) {
+          tma_load_3d_pf(kd + cb * C::kKVCB + lane * 2048, &pp.tmap_k, 64 * cb, g, row, &kv_full[s]);
+          tma_load_3d_pf(vd + cb * C::kKVCB + lane * 2048, &pp.tmap_v, 64 * cb, g, row, &kv_full[s]);
+        }
+      }
+      issued = j + 1;
+    }
+    // never leave copies in flight into this CTA's shared memory (even after an abort)
+    for (int j = max(0, issued - 2); j < issued; ++j)
+      mbar_wait_bounded(&kv_full[j & 1], (j >> 1) & 1, p.status, DEV_TIMEOUT);
+    if (lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
+  } else if (warp == 5) {
+    // ======================================================== MMA issuer
+    constexpr uint32_t kIdQK = umma_idesc_f16(128, BN, BF16, false);
+    constexpr uint32_t kIdPV = umma_idesc_f16(128, D, BF16, true);
+    bool ok = pf_wait(q_full, 0, abort_flag, p.status);
+    auto do_pv = [&](int i) -> bool {
+      if (!pf_wait(p_full, i & 1, abort_flag, p.status)) return false;
+      tc_fence_after();
+      const bool use_lo = BF16 && lo_flag[i & 1] == i + 1;
+      uint8_t* vs = sKV + (i & 1) * C::kStageBytes + C::kCB * C::kKVCB;
+      if (lane == 0) {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          if (part == 1 && !use_lo) break;
+          const uint32_t pbase = smem_addr(sP + part * C::kPBytes);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t ad =
+                smem_desc_sw128(pbase + (kk >> 2) * C::kPCB + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(smem_addr(vs) + kk * 16 * 128, C::kKVCB, 1024);
+            umma_f16_ss(tO, ad, bd, kIdPV, (i > 0 || kk > 0 || part > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(pv_done);
+        umma_commit(&kv_empty[i & 1]);
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; ok && j < nt; ++j) {
+      const int s = j & 1;
+      if (!pf_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      // Cache slots at or past kv_len hold no key and may hold anything (NaN included):
+      // zero those V rows before the tensor cores multiply them by P = 0.
+      const int k0 = ks + j * BN;
+      if (k0 + BN > kv_len) {
+        uint8_t* vs = sKV + s * C::kStageBytes + C::kCB * C::kKVCB;
+        const int r_lo = max(0, kv_len - k0), r_hi = min(BN, ((kv_len + 15) & ~15) - k0);
+        for (int i = lane; i < (r_hi - r_lo) * C::kCB * 8; i += 32) {
+          const int r = r_lo + i / (C::kCB * 8), c = i % (C::kCB * 8);
+          *reinterpret_cast<uint4*>(vs + (c / 8) * C::kKVCB + r * 128 + (c % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (j >= 2 && !pf_wait(&s_free[s], ((j >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t qb = smem_addr(sQ);
+        const uint32_t kb = smem_addr(sKV + s * C::kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kKVCB + (kk & 3) * 32, 16, 1024);
+          umma_f16_ss(tS[s], ad, bd, kIdQK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[s]);
+      }
+      __syncwarp();
+      if (j >= 1 && !do_pv(j - 1)) { ok = false; break; }
+    }
+    if (ok && nt > 0) do_pv(nt - 1);
+    // nothing may still be in flight on the tensor cores when the memory is freed
+    if (lane == 0) umma_commit(fin);
+    __syncwarp();
+    mbar_wait_bounded(fin, 0, p.status, DEV_TIMEOUT);
+  } else {
+    // ======================================================== softmax warps (thread = row)
+    const int r = 32 * warp + lane;
+    const int tl = r / G;                                  // token within the block
+    const bool rv = r < rows && q0 + t_first + tl < p.total_q;
+    const int i_q = t_first + (rv ? tl : 0);               // query index within the sequence
+    const int h = g * G + r % G;
+    const int pos = ctx + i_q;
+    const int lo_r = p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
+    // warp-uniform bounds of this warp's valid rows, to mask only boundary tiles
+    int pmin = rv ? pos : INT_MAX, lomax = rv ? lo_r : INT_MIN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
+      lomax = max(lomax, __shfl_xor_sync(0xffffffffu, lomax, o));
+    }
+    const float scale_log2 = p.scale * kLog2e;
+    const float inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+    float slope = 0.f;
+    const float* qq_row = nullptr;
+    if constexpr (FEAT) {
+      if (p.alibi != nullptr && rv) slope = __ldg(p.alibi + h);
+      if (p.qq_bias != nullptr && rv && i_q < p.max_seqlen_q)
+        qq_row = p.qq_bias + static_cast<size_t>(i_q) * p.qq_stride;
+    }
+    const bool sink = p.sinks != nullptr && z == 0 && rv;
+    float m_used = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+    float l = sink ? 1.f : 0.f;
+    const uint32_t lane_off = (32u * warp) << 16;
+    bool ok = true;
+    uint8_t* const pw_hi = sP + r * 128;
+    uint8_t* const pw_lo = sP + C::kPBytes + r * 128;
+
+    for (int j = 0; j < nt; ++j) {
+      const int s = j & 1;
+      if (!pf_wait(&s_full[s], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      float x[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tS[s] + lane_off + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c0 + e] = __uint_as_float(rr[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[s]);
+
+      // ---- scale, softcap, biases, mask (log2 domain)
+      const int k0 = ks + j * BN;
+      const bool need_mask = k0 < lomax || k0 + BN - 1 > pmin || k0 + BN > ke;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BN; ++e) {
+        const int jk = k0 + e;
+        float v;
+        if constexpr (FEAT) {
+          v = x[e] * p.scale;
+          if (p.softcap > 0.f) v = p.softcap * tanhf(v * inv_softcap);
+          v += slope * static_cast<float>(jk - ctx);
+          if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
+          v *= kLog2e;
+        } else {
+          v = x[e] * scale_log2;
+        }
+        if (need_mask) v = (rv && jk >= lo_r && jk <= pos && jk < ke) ? v : -INFINITY;
+        x[e] = v;
+        mx = fmaxf(mx, v);
+      }
+      // ---- running max, used lazily: O and l are rescaled only when the max grows by
+      // more than 8 in log2 units (P stays <= 256, far inside the fp32 and P ranges)
+      float alpha = 1.f;
+      const bool grow = mx > m_used + 8.f || (m_used == -INFINITY && mx > -INFINITY);
+      if (grow) {
+        alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mx);
+        m_used = mx;
+      }
+      const float m_use = m_used == -INFINITY ? 0.f : m_used;
+      float rs = 0.f, pmax = 0.f;
+#pragma unroll
+      for (int e = 0; e < BN; ++e) {
+        x[e] = fast_exp2(x[e] - m_use);
+        rs += x[e];
+        pmax = fmaxf(pmax, x[e]);
+      }
+      l = l * alpha + rs;
+      // the low part of P matters only where one key can still weigh more than 1/64
+      const bool need_lo = BF16 && pmax * 64.f > l;
+
+      // ---- P buffer free and O final for tile j-1
+      if (j >= 1) {
+        if (!pf_wait(pv_done, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tO + lane_off + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st32(tO + lane_off + c0, rr);
+        }
+        tmem_st_wait();
+      }
+      // ---- P rows to shared memory (128-byte swizzled, K-major A operand)
+#pragma unroll
+      for (int c = 0; c < BN / 8; ++c) {
+        uint32_t hi4[4], lo4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float a0 = x[8 * c + 2 * q], a1 = x[8 * c + 2 * q + 1];
+          if constexpr (BF16) {
+            hi4[q] = pack_bf16(a0, a1);
+            lo4[q] = pack_bf16(a0 - bf16_lo(hi4[q]), a1 - bf16_hi(hi4[q]));
+          } else {
+            hi4[q] = pack_f16(a0, a1);
+          }
+        }
+        const uint32_t off = (c >> 3) * C::kPCB + ((((c & 7) ^ (r & 7))) << 4);
+        *reinterpret_cast<uint4*>(pw_hi + off) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
+        if constexpr (BF16)
+          *reinterpret_cast<uint4*>(pw_lo + off) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+      }
+      if (BF16 && __any_sync(0xffffffffu, need_lo) && lane == 0) lo_flag[j & 1] = j + 1;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+
+    // ---- epilogue: O / l for one partition, or the partition's max / sum / O
+    if (ok && nt > 0) ok = pf_wait(pv_done, (nt - 1) & 1, abort_flag, p.status);
+    tc_fence_after();
+    if (ok) {
+      const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
+      const size_t n_part = static_cast<size_t>(p.n_part);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t rr[32];
+        if (nt > 0) {
+          tmem_ld32(tO + lane_off + c0, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = 0u;
+        }
+        if (!rv) continue;
+        if (n_part == 1) {
+          if (p.out_dtype == UA_DT_F32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + c0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(rr[4 * e]) * inv, __uint_as_float(rr[4 * e + 1]) * inv,
+                                   __uint_as_float(rr[4 * e + 2]) * inv, __uint_as_float(rr[4 * e + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * D + c0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint32_t w[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float a0 = __uint_as_float(rr[8 * e + 2 * q]) * inv;
+                const float a1 = __uint_as_float(rr[8 * e + 2 * q + 1]) * inv;
+                w[q] = p.out_dtype == UA_DT_BF16 ? pack_bf16(a0, a1) : pack_f16(a0, a1);
+              }
+              dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else {
+          const size_t w = orow * n_part + z;
+          if (c0 == 0) {
+            p.ws_m[w] = m_used;
+            p.ws_l[w] = l;
+          }
+          float4* dst = reinterpret_cast<float4*>(p.ws_acc + w * D + c0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
+                                 __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D, bool BF16, bool FEAT>
+cudaError_t launch_prefill_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
+  using C = PrefillCfg<D>;
+  auto kern = ua_prefill_tc_kernel<D, BF16, FEAT>;
+  static std::atomic<unsigned long long> configured{0};  // one bit per device
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    configured.fetch_or(bit);
+  }
+  return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, 1, pp);
+}
+
+template <int D>
+cudaError_t launch_prefill_dispatch(const PrefillParams& pp, dim3 grid, int kv, bool feat,
+                                    cudaStream_t s) {
+  if (kv == KV_BF16)
+    return feat ? launch_prefill_t<D, true, true>(pp, grid, s) : launch_prefill_t<D, true, false>(pp, grid, s);
+  if (kv == KV_F16)
+    return feat ? launch_prefill_t<D, false, true>(pp, grid, s) : launch_prefill_t<D, false, false>(pp, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ua
