@@ -20,8 +20,9 @@
 // memory round trips rare.
 //
 // Warp roles (192 threads):  warps 0..3 softmax + epilogue (thread = row = TMEM lane),
-// warp 4 TMA producer (Q once, then K/V pages of 16 keys through the block table into a
-// 2-stage ring, 128-byte swizzled), warp 5 MMA issuer and tensor-memory owner.
+// warp 4 TMA producer (Q once, then K and V pages of 16 keys through the block table into
+// two separate rings, 128-byte swizzled: a K slot is refilled as soon as its QK^T is done,
+// a V slot once its P.V is done), warp 5 MMA issuer and tensor-memory owner.
 #pragma once
 
 #include <atomic>
@@ -39,20 +40,23 @@ namespace ua {
 template <int D>
 struct PrefillCfg {
   static constexpr int kBM = 128;                        // MMA rows
-  static constexpr int kBN = D >= 256 ? 64 : 128;        // keys per tile
+  static constexpr int kBN = 64;                         // keys per tile
   static constexpr int kCB = D / 64;                     // 128-byte column blocks of a row
   static constexpr int kQBytes = kCB * kBM * 128;
   static constexpr int kKVCB = kBN * 128;                // one column block of a K or V tile
-  static constexpr int kStageBytes = 2 * kCB * kKVCB;    // K then V
-  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = kCB * kKVCB;         // one K (or V) tile
   static constexpr int kPCB = kBM * 128;                 // one column block (64 keys) of P
   static constexpr int kPBytes = (kBN / 64) * kPCB;
+  // ring depth: as many K and V tiles as fit beside Q and P (at most 4 each)
+  static constexpr int kFree = 227 * 1024 - 1024 - 256 - kQBytes - 2 * kPBytes;
+  static constexpr int kRing = kFree / (2 * kTileBytes) > 4 ? 4 : kFree / (2 * kTileBytes);
   static constexpr int kSmemBytes =
-      1024 + kQBytes + kStages * kStageBytes + 2 * kPBytes + 256;
+      1024 + kQBytes + 2 * kRing * kTileBytes + 2 * kPBytes + 256;
   static constexpr int kTmemCols = 512;                  // S0, S1, O  (2*BN + D <= 512)
   static constexpr int kThreads = 192;
   static_assert(2 * kBN + D <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kRing >= 2, "at least double-buffered K and V");
 };
 
 __device__ __forceinline__ void tma_load_3d_pf(void* dst, const CUtensorMap* map, int x, int y,
@@ -103,21 +107,25 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int R = C::kRing;
   uint8_t* const sQ = smem;
-  uint8_t* const sKV = sQ + C::kQBytes;
-  uint8_t* const sP = sKV + C::kStages * C::kStageBytes;  // P high part, then P low part
+  uint8_t* const sK = sQ + C::kQBytes;               // R K tiles
+  uint8_t* const sV = sK + R * C::kTileBytes;        // R V tiles
+  uint8_t* const sP = sV + R * C::kTileBytes;        // P high part, then P low part
   uint64_t* const bars = reinterpret_cast<uint64_t*>(sP + 2 * C::kPBytes);
   uint64_t* const q_full = bars + 0;
-  uint64_t* const kv_full = bars + 1;   // [2]
-  uint64_t* const kv_empty = bars + 3;  // [2]
-  uint64_t* const s_full = bars + 5;    // [2]
-  uint64_t* const s_free = bars + 7;    // [2]
-  uint64_t* const p_full = bars + 9;
-  uint64_t* const pv_done = bars + 10;
-  uint64_t* const fin = bars + 11;
-  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(bars + 12);
-  int* const lo_flag = reinterpret_cast<int*>(bars + 13);  // [2]: tile index + 1 when the
-                                                            // low part of P matters
+  uint64_t* const s_full = bars + 1;    // [2]
+  uint64_t* const s_free = bars + 3;    // [2]
+  uint64_t* const p_full = bars + 5;
+  uint64_t* const pv_done = bars + 6;
+  uint64_t* const fin = bars + 7;
+  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
+  int* const lo_flag = reinterpret_cast<int*>(bars + 9);  // [2]: tile index + 1 when the
+                                                           // low part of P matters
+  uint64_t* const k_full = bars + 10;   // [R]
+  uint64_t* const k_empty = bars + 14;  // [R]
+  uint64_t* const v_full = bars + 18;   // [R]
+  uint64_t* const v_empty = bars + 22;  // [R]
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
@@ -150,11 +158,15 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
       lo_flag[i] = 0;
+    }
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
@@ -205,26 +217,33 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
     int row_next = nt > 0 ? page_row(0) : oob;
     int issued = 0;
     for (int j = 0; j < nt; ++j) {
-      const int s = j & 1;
+      const int s = j % R;
+      const uint32_t ph = ((j / R) - 1) & 1;  // phase of the release of tile j - R
       const int row = row_next;
       if (j + 1 < nt) row_next = page_row(j + 1);
-      if (j >= 2 && !pf_wait(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.status)) break;
-      uint8_t* kd = sKV + s * C::kStageBytes;
-      uint8_t* vd = kd + C::kCB * C::kKVCB;
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
+      if (j >= R && !pf_wait(&k_empty[s], ph, abort_flag, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
       __syncwarp();
-      if (lane < BN / 16) {
+      if (lane < BN / 16)
 #pragma unroll
-        for (int cb = 0; cb < C::kCB; ++cb) {
-          tma_load_3d_pf(kd + cb * C::kKVCB + lane * 2048, &pp.tmap_k, 64 * cb, g, row, &kv_full[s]);
-          tma_load_3d_pf(vd + cb * C::kKVCB + lane * 2048, &pp.tmap_v, 64 * cb, g, row, &kv_full[s]);
-        }
-      }
+        for (int cb = 0; cb < C::kCB; ++cb)
+          tma_load_3d_pf(sK + s * C::kTileBytes + cb * C::kKVCB + lane * 2048, &pp.tmap_k,
+                         64 * cb, g, row, &k_full[s]);
+      if (j >= R && !pf_wait(&v_empty[s], ph, abort_flag, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+      __syncwarp();
+      if (lane < BN / 16)
+#pragma unroll
+        for (int cb = 0; cb < C::kCB; ++cb)
+          tma_load_3d_pf(sV + s * C::kTileBytes + cb * C::kKVCB + lane * 2048, &pp.tmap_v,
+                         64 * cb, g, row, &v_full[s]);
       issued = j + 1;
     }
     // never leave copies in flight into this CTA's shared memory (even after an abort)
-    for (int j = max(0, issued - 2); j < issued; ++j)
-      mbar_wait_bounded(&kv_full[j & 1], (j >> 1) & 1, p.status, DEV_TIMEOUT);
+    for (int j = max(0, issued - R); j < issued; ++j) {
+      mbar_wait_bounded(&k_full[j % R], (j / R) & 1, p.status, DEV_TIMEOUT);
+      mbar_wait_bounded(&v_full[j % R], (j / R) & 1, p.status, DEV_TIMEOUT);
+    }
     if (lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
   } else if (warp == 5) {
     // ======================================================== MMA issuer
@@ -232,10 +251,25 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
     constexpr uint32_t kIdPV = umma_idesc_f16(128, D, BF16, true);
     bool ok = pf_wait(q_full, 0, abort_flag, p.status);
     auto do_pv = [&](int i) -> bool {
+      const int vs_i = i % R;
+      if (!pf_wait(&v_full[vs_i], (i / R) & 1, abort_flag, p.status)) return false;
+      uint8_t* vs = sV + vs_i * C::kTileBytes;
+      // Cache slots at or past kv_len hold no key and may hold anything (NaN included):
+      // zero those V rows before the tensor cores multiply them by P = 0.
+      const int k0 = ks + i * BN;
+      if (k0 + BN > kv_len) {
+        const int r_lo = max(0, kv_len - k0), r_hi = min(BN, ((kv_len + 15) & ~15) - k0);
+        for (int e = lane; e < (r_hi - r_lo) * C::kCB * 8; e += 32) {
+          const int r = r_lo + e / (C::kCB * 8), c = e % (C::kCB * 8);
+          *reinterpret_cast<uint4*>(vs + (c / 8) * C::kKVCB + r * 128 + (c % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (!pf_wait(p_full, i & 1, abort_flag, p.status)) return false;
       tc_fence_after();
       const bool use_lo = BF16 && lo_flag[i & 1] == i + 1;
-      uint8_t* vs = sKV + (i & 1) * C::kStageBytes + C::kCB * C::kKVCB;
       if (lane == 0) {
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -250,33 +284,20 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
           }
         }
         umma_commit(pv_done);
-        umma_commit(&kv_empty[i & 1]);
+        umma_commit(&v_empty[vs_i]);
       }
       __syncwarp();
       return true;
     };
     for (int j = 0; ok && j < nt; ++j) {
+      const int ks_j = j % R;
+      if (!pf_wait(&k_full[ks_j], (j / R) & 1, abort_flag, p.status)) { ok = false; break; }
       const int s = j & 1;
-      if (!pf_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      // Cache slots at or past kv_len hold no key and may hold anything (NaN included):
-      // zero those V rows before the tensor cores multiply them by P = 0.
-      const int k0 = ks + j * BN;
-      if (k0 + BN > kv_len) {
-        uint8_t* vs = sKV + s * C::kStageBytes + C::kCB * C::kKVCB;
-        const int r_lo = max(0, kv_len - k0), r_hi = min(BN, ((kv_len + 15) & ~15) - k0);
-        for (int i = lane; i < (r_hi - r_lo) * C::kCB * 8; i += 32) {
-          const int r = r_lo + i / (C::kCB * 8), c = i % (C::kCB * 8);
-          *reinterpret_cast<uint4*>(vs + (c / 8) * C::kKVCB + r * 128 + (c % 8) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
       if (j >= 2 && !pf_wait(&s_free[s], ((j >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
         const uint32_t qb = smem_addr(sQ);
-        const uint32_t kb = smem_addr(sKV + s * C::kStageBytes);
+        const uint32_t kb = smem_addr(sK + ks_j * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
@@ -284,6 +305,7 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
           umma_f16_ss(tS[s], ad, bd, kIdQK, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[s]);
+        umma_commit(&k_empty[ks_j]);
       }
       __syncwarp();
       if (j >= 1 && !do_pv(j - 1)) { ok = false; break; }
@@ -325,6 +347,7 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
     bool ok = true;
     uint8_t* const pw_hi = sP + r * 128;
     uint8_t* const pw_lo = sP + C::kPBytes + r * 128;
+    bool lo_dirty = true;  // the low P rows of this thread hold something other than zeros
 
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1;
@@ -343,27 +366,38 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[s]);
 
-      // ---- scale, softcap, biases, mask (log2 domain)
+      // ---- scores: with no softcap or bias the log2-domain score is c * s with
+      // c = scale * log2(e) > 0, so the row max is taken on the raw dot products and the
+      // scale is folded into the exponent's FMA; softcap and biases are applied first
       const int k0 = ks + j * BN;
       const bool need_mask = k0 < lomax || k0 + BN - 1 > pmin || k0 + BN > ke;
-      float mx = -INFINITY;
+      float c = scale_log2;
+      if constexpr (FEAT) {
+        c = kLog2e;
 #pragma unroll
-      for (int e = 0; e < BN; ++e) {
-        const int jk = k0 + e;
-        float v;
-        if constexpr (FEAT) {
-          v = x[e] * p.scale;
+        for (int e = 0; e < BN; ++e) {
+          const int jk = k0 + e;
+          float v = x[e] * p.scale;
           if (p.softcap > 0.f) v = p.softcap * tanhf(v * inv_softcap);
           v += slope * static_cast<float>(jk - ctx);
           if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
-          v *= kLog2e;
-        } else {
-          v = x[e] * scale_log2;
+          x[e] = v;
         }
-        if (need_mask) v = (rv && jk >= lo_r && jk <= pos && jk < ke) ? v : -INFINITY;
-        x[e] = v;
-        mx = fmaxf(mx, v);
       }
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const int jk = k0 + e;
+          x[e] = (rv && jk >= lo_r && jk <= pos && jk < ke) ? x[e] : -INFINITY;
+        }
+      }
+      float mx0 = x[0], mx1 = x[1];
+#pragma unroll
+      for (int e = 2; e < BN; e += 2) {
+        mx0 = fmaxf(mx0, x[e]);
+        mx1 = fmaxf(mx1, x[e + 1]);
+      }
+      const float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
       // ---- running max, used lazily: O and l are rescaled only when the max grows by
       // more than 8 in log2 units (P stays <= 256, far inside the fp32 and P ranges)
       float alpha = 1.f;
@@ -373,13 +407,22 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
         m_used = mx;
       }
       const float m_use = m_used == -INFINITY ? 0.f : m_used;
-      float rs = 0.f, pmax = 0.f;
+      // ---- P = 2^(c s - m): one packed FMA per two scores, one ex2 per score
+      const float2 cc = make_float2(c, c), mm = make_float2(-m_use, -m_use);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < BN; ++e) {
-        x[e] = fast_exp2(x[e] - m_use);
-        rs += x[e];
-        pmax = fmaxf(pmax, x[e]);
+      for (int e = 0; e < BN; e += 4) {
+        const float2 u = __ffma2_rn(make_float2(x[e], x[e + 1]), cc, mm);
+        const float2 w = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), cc, mm);
+        x[e] = fast_exp2(u.x);
+        x[e + 1] = fast_exp2(u.y);
+        x[e + 2] = fast_exp2(w.x);
+        x[e + 3] = fast_exp2(w.y);
+        acc0 = __fadd2_rn(acc0, make_float2(x[e], x[e + 1]));
+        acc1 = __fadd2_rn(acc1, make_float2(x[e + 2], x[e + 3]));
       }
+      const float rs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+      const float pmax = mx == -INFINITY ? 0.f : fast_exp2(mx - m_use);  // largest P of the row
       l = l * alpha + rs;
       // the low part of P matters only where one key can still weigh more than 1/64
       const bool need_lo = BF16 && pmax * 64.f > l;
@@ -401,26 +444,36 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
         }
         tmem_st_wait();
       }
-      // ---- P rows to shared memory (128-byte swizzled, K-major A operand)
+      // ---- P rows to shared memory (128-byte swizzled, K-major A operand).  The low
+      // part is computed only by warps with a row that needs it; a warp that does not
+      // keeps zeros in its low rows (written once), so the MMA may use the low buffer
+      // whenever any warp asks for it.
+      const bool warp_lo = BF16 && __any_sync(0xffffffffu, need_lo);
 #pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        uint32_t hi4[4], lo4[4];
+      for (int cq = 0; cq < BN / 8; ++cq) {
+        uint32_t hi4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float a0 = x[8 * c + 2 * q], a1 = x[8 * c + 2 * q + 1];
-          if constexpr (BF16) {
-            hi4[q] = pack_bf16(a0, a1);
-            lo4[q] = pack_bf16(a0 - bf16_lo(hi4[q]), a1 - bf16_hi(hi4[q]));
-          } else {
-            hi4[q] = pack_f16(a0, a1);
-          }
+          const float a0 = x[8 * cq + 2 * q], a1 = x[8 * cq + 2 * q + 1];
+          hi4[q] = BF16 ? pack_bf16(a0, a1) : pack_f16(a0, a1);
         }
-        const uint32_t off = (c >> 3) * C::kPCB + ((((c & 7) ^ (r & 7))) << 4);
+        const uint32_t off = (cq >> 3) * C::kPCB + ((((cq & 7) ^ (r & 7))) << 4);
         *reinterpret_cast<uint4*>(pw_hi + off) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
-        if constexpr (BF16)
+        if (BF16 && warp_lo) {
+          uint32_t lo4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 rem = __fadd2_rn(make_float2(x[8 * cq + 2 * q], x[8 * cq + 2 * q + 1]),
+                                          make_float2(-bf16_lo(hi4[q]), -bf16_hi(hi4[q])));
+            lo4[q] = pack_bf16(rem.x, rem.y);
+          }
           *reinterpret_cast<uint4*>(pw_lo + off) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+        } else if (BF16 && lo_dirty) {
+          *reinterpret_cast<uint4*>(pw_lo + off) = make_uint4(0, 0, 0, 0);
+        }
       }
-      if (BF16 && __any_sync(0xffffffffu, need_lo) && lane == 0) lo_flag[j & 1] = j + 1;
+      if (BF16) lo_dirty = warp_lo;
+      if (warp_lo && lane == 0) lo_flag[j & 1] = j + 1;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
