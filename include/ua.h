@@ -108,7 +108,8 @@ typedef struct {
   int32_t kernel;      /* 1: warp-MMA tile kernel, 16 rows per CTA (decode-shaped q-blocks);
                           4: warp-MMA tile kernel, 64 rows per CTA (fp8 caches, block sizes
                           not a multiple of 16); 8: tensor-memory (tcgen05) kernel with
-                          128-row q-blocks of floor(128 / G) tokens x G heads */
+                          128-row q-blocks of floor(128 / G) tokens x G heads; 16: the same
+                          kernel with two such tiles of consecutive tokens per CTA */
   int32_t block_m;     /* (query token x head) rows per q-block */
   int32_t n_part;      /* key-range partitions (1 on the 2D path) */
   int32_t grid_x;      /* q-block slots: num_seqs when slot_per_seq, else

@@ -130,8 +130,11 @@ int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, in
 //
 // Kernel: decode-shaped calls (every sequence's rows fit 16) take the warp-MMA tile kernel
 // with 16-row q-blocks; other calls on fp16/bf16 caches with 16 | block_size take the
-// tensor-memory kernel with 128-row q-blocks (floor(128 / G) tokens x G heads); the rest
-// (fp8 caches, other block sizes) take the tile kernel with 64-row q-blocks.
+// tensor-memory kernel with 128-row q tiles (floor(128 / G) tokens x G heads), two tiles
+// per CTA for head_dim <= 128 when that grid still fills the device; the rest (fp8
+// caches, other block sizes) take the tile kernel with 64-row q-blocks.
+bool is_tc(int kernel) { return kernel == ua::KERNEL_TC128 || kernel == ua::KERNEL_TC256; }
+
 void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int window_left,
                int kv_dtype, int backend, int num_sms, bool allow_tc, ua_plan_t* pl) {
   const int group = hq / hkv;
@@ -139,12 +142,18 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
   const bool tc = allow_tc && rows_max > 16 && group <= 128 && block_size % 16 == 0 &&
                   (kv_dtype == UA_DT_F16 || kv_dtype == UA_DT_BF16);
   const int wm = rows_max <= 16 ? 1 : 4;
-  const int tq = tc ? 128 / group : 0;               // tokens per tensor-memory q-block
-  const int bm = tc ? tq * group : ua::tile_block_m(wm);
+  const int tq = tc ? 128 / group : 0;               // tokens per 128-row tensor-memory tile
+  // two tiles per CTA (sharing every K/V tile) where their tensor memory fits and the
+  // grid still fills the device
+  const int nq = tc && d <= 128 &&
+                         (static_cast<long long>(sh->total_q) / (2 * tq) + sh->num_seqs) * hkv >= num_sms
+                     ? 2
+                     : 1;
+  const int bm = tc ? nq * tq * group : ua::tile_block_m(wm);
   // every sequence fits one q-block: slot x is sequence x; else the monotone slot layout
   const bool per_seq = !tc && rows_max <= bm;
   const long long slots =
-      tc ? static_cast<long long>(sh->total_q) / tq + sh->num_seqs
+      tc ? static_cast<long long>(sh->total_q) / (nq * tq) + sh->num_seqs
          : per_seq ? sh->num_seqs
                    : static_cast<long long>(sh->total_q) * group / bm + sh->num_seqs;
   const long long active = per_seq ? std::min<long long>(sh->num_seqs, sh->total_q) : slots;
@@ -165,7 +174,7 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
   }
   n_part = std::min(n_part, kMaxPartitions);
   pl->path = n_part > 1 ? UA_PATH_SPLIT : UA_PATH_2D;
-  pl->kernel = tc ? ua::KERNEL_TC128 : wm;
+  pl->kernel = tc ? (nq == 2 ? ua::KERNEL_TC256 : ua::KERNEL_TC128) : wm;
   pl->block_m = bm;
   pl->n_part = n_part;
   pl->grid_x = static_cast<int32_t>(slots);
@@ -293,7 +302,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   // The tensor-memory kernel needs TMA maps of q and both caches; if one cannot be made,
   // the call is planned again for the tile kernel.
   ua::PrefillParams pp{};
-  if (pl.kernel == ua::KERNEL_TC128) {
+  if (is_tc(pl.kernel)) {
     const int group = hq / hkv;
     const bool maps =
         static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX &&
@@ -321,7 +330,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   }
   const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
   // Page-sized TMA boxes need 16 | block_size and row coordinates that fit in int32.
-  bool tma = pl.kernel != ua::KERNEL_TC128 && block_size % 16 == 0 &&
+  bool tma = !is_tc(pl.kernel) && block_size % 16 == 0 &&
              static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
   if (tma)
     tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
@@ -329,12 +338,13 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(sh->events);
   if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return UA_ERR_CUDA;
   cudaError_t err;
-  if (pl.kernel == ua::KERNEL_TC128) {
+  if (is_tc(pl.kernel)) {
     pp.p = p;
+    const int nq = pl.kernel == ua::KERNEL_TC256 ? 2 : 1;
     switch (d) {
-      case 64: err = ua::launch_prefill_d64(pp, grid, kv, feat, st); break;
-      case 128: err = ua::launch_prefill_d128(pp, grid, kv, feat, st); break;
-      default: err = ua::launch_prefill_d256(pp, grid, kv, feat, st); break;
+      case 64: err = ua::launch_prefill_d64(pp, grid, kv, feat, nq, st); break;
+      case 128: err = ua::launch_prefill_d128(pp, grid, kv, feat, nq, st); break;
+      default: err = ua::launch_prefill_d256(pp, grid, kv, feat, nq, st); break;
     }
   } else switch (d) {
     case 64: err = ua::launch_tile_d64(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;

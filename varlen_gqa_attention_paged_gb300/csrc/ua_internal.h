@@ -50,7 +50,8 @@ struct TileParams {
 
 // Tensor-memory prefill kernel launch argument: tensor maps of q viewed as
 // [total_q][H_q][D] (box: 64 elements x G heads x tq tokens) and of the two caches, the
-// attention parameters, and tq = query tokens per 128-row q-block (floor(128 / G)).
+// attention parameters, and tq = query tokens per 128-row q tile (floor(128 / G)); a CTA
+// owns 1 or 2 such tiles of consecutive tokens.
 struct PrefillParams {
   CUtensorMap tmap_q;
   CUtensorMap tmap_k;
@@ -81,12 +82,15 @@ cudaError_t launch_tile_d128(const TileParams& tp, dim3 grid, int wm, int kv, bo
 cudaError_t launch_tile_d256(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
                              int cluster_y, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
-cudaError_t launch_prefill_d64(const PrefillParams& pp, dim3 grid, int kv, bool feat, cudaStream_t s);
-cudaError_t launch_prefill_d128(const PrefillParams& pp, dim3 grid, int kv, bool feat, cudaStream_t s);
-cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool feat, cudaStream_t s);
+cudaError_t launch_prefill_d64(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
+                               cudaStream_t s);
+cudaError_t launch_prefill_d128(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
+                               cudaStream_t s);
+cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
+                               cudaStream_t s);
 
 // Plan kernel codes.
-enum : int { KERNEL_TILE16 = 1, KERNEL_TILE64 = 4, KERNEL_TC128 = 8 };
+enum : int { KERNEL_TILE16 = 1, KERNEL_TILE64 = 4, KERNEL_TC128 = 8, KERNEL_TC256 = 16 };
 
 // Resident CTAs per SM of the tile kernel variant for (head_dim, kv dtype, wm).
 int tile_ctas_per_sm(int head_dim, int kv, int wm);

@@ -37,27 +37,33 @@
 
 namespace ua {
 
-template <int D>
+template <int D, int NQ>
 struct PrefillCfg {
-  static constexpr int kBM = 128;                        // MMA rows
+  static constexpr int kBM = 128;                        // MMA rows of one q tile
   static constexpr int kBN = 64;                         // keys per tile
   static constexpr int kCB = D / 64;                     // 128-byte column blocks of a row
-  static constexpr int kQBytes = kCB * kBM * 128;
+  static constexpr int kQBytes = kCB * kBM * 128;        // one q tile
   static constexpr int kKVCB = kBN * 128;                // one column block of a K or V tile
   static constexpr int kTileBytes = kCB * kKVCB;         // one K (or V) tile
   static constexpr int kPCB = kBM * 128;                 // one column block (64 keys) of P
-  static constexpr int kPBytes = (kBN / 64) * kPCB;
+  static constexpr int kPBytes = (kBN / 64) * kPCB;      // P of one q tile (one part)
+  static constexpr int kBarBytes = 512;
   // ring depth: as many K and V tiles as fit beside Q and P (at most 4 each)
-  static constexpr int kFree = 227 * 1024 - 1024 - 256 - kQBytes - 2 * kPBytes;
+  static constexpr int kFree = 227 * 1024 - 1024 - kBarBytes - NQ * kQBytes - NQ * 2 * kPBytes;
   static constexpr int kRing = kFree / (2 * kTileBytes) > 4 ? 4 : kFree / (2 * kTileBytes);
   static constexpr int kSmemBytes =
-      1024 + kQBytes + 2 * kRing * kTileBytes + 2 * kPBytes + 256;
-  static constexpr int kTmemCols = 512;                  // S0, S1, O  (2*BN + D <= 512)
-  static constexpr int kThreads = 192;
-  static_assert(2 * kBN + D <= kTmemCols, "tensor memory budget");
+      1024 + NQ * kQBytes + 2 * kRing * kTileBytes + NQ * 2 * kPBytes + kBarBytes;
+  static constexpr int kTmemStride = 2 * kBN + D;        // S0, S1, O of one q tile
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSoftmaxWarps = 4 * NQ;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 64;
+  static_assert(NQ * kTmemStride <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kRing >= 2, "at least double-buffered K and V");
 };
+
+// Two q tiles per CTA need 2 x (S0, S1, O) columns of tensor memory.
+constexpr bool prefill_two_tiles_fit(int d) { return 2 * (2 * 64 + d) <= 512; }
 
 __device__ __forceinline__ void tma_load_3d_pf(void* dst, const CUtensorMap* map, int x, int y,
                                                int z, uint64_t* bar) {
@@ -96,10 +102,13 @@ __device__ __forceinline__ int pf_find_seq(const int32_t* __restrict__ cu, int n
   return lo;
 }
 
-template <int D, bool BF16, bool FEAT>
-__global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_constant__ PrefillParams pp) {
-  using C = PrefillCfg<D>;
+template <int D, int NQ, bool BF16, bool FEAT>
+__global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
+    ua_prefill_tc_kernel(const __grid_constant__ PrefillParams pp) {
+  using C = PrefillCfg<D, NQ>;
   constexpr int BN = C::kBN;
+  constexpr int R = C::kRing;
+  constexpr int kProducer = C::kSoftmaxWarps, kMma = C::kSoftmaxWarps + 1;
   const AttnParams& p = pp.p;
   grid_dependency_wait();
   grid_launch_dependents();
@@ -107,25 +116,25 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr int R = C::kRing;
-  uint8_t* const sQ = smem;
-  uint8_t* const sK = sQ + C::kQBytes;               // R K tiles
+  uint8_t* const sQ = smem;                          // NQ q tiles
+  uint8_t* const sK = sQ + NQ * C::kQBytes;          // R K tiles
   uint8_t* const sV = sK + R * C::kTileBytes;        // R V tiles
-  uint8_t* const sP = sV + R * C::kTileBytes;        // P high part, then P low part
-  uint64_t* const bars = reinterpret_cast<uint64_t*>(sP + 2 * C::kPBytes);
+  uint8_t* const sP = sV + R * C::kTileBytes;        // per q tile: P high part, P low part
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(sP + NQ * 2 * C::kPBytes);
   uint64_t* const q_full = bars + 0;
-  uint64_t* const s_full = bars + 1;    // [2]
-  uint64_t* const s_free = bars + 3;    // [2]
-  uint64_t* const p_full = bars + 5;
-  uint64_t* const pv_done = bars + 6;
-  uint64_t* const fin = bars + 7;
-  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
-  int* const lo_flag = reinterpret_cast<int*>(bars + 9);  // [2]: tile index + 1 when the
-                                                           // low part of P matters
-  uint64_t* const k_full = bars + 10;   // [R]
-  uint64_t* const k_empty = bars + 14;  // [R]
-  uint64_t* const v_full = bars + 18;   // [R]
-  uint64_t* const v_empty = bars + 22;  // [R]
+  uint64_t* const fin = bars + 1;
+  uint64_t* const k_full = bars + 2;            // [R]
+  uint64_t* const k_empty = bars + 2 + R;       // [R]
+  uint64_t* const v_full = bars + 2 + 2 * R;    // [R]
+  uint64_t* const v_empty = bars + 2 + 3 * R;   // [R]
+  uint64_t* const tile_bars = bars + 2 + 4 * R; // [NQ][6]: s_full[2], s_free[2], p_full, pv_done
+  auto s_full = [&](int qt, int s) { return tile_bars + 6 * qt + s; };
+  auto s_free = [&](int qt, int s) { return tile_bars + 6 * qt + 2 + s; };
+  auto p_full = [&](int qt) { return tile_bars + 6 * qt + 4; };
+  auto pv_done = [&](int qt) { return tile_bars + 6 * qt + 5; };
+  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(tile_bars + 6 * NQ);
+  // [NQ][2]: walk step + 1 of the tile's P when its low part matters
+  int* const lo_flag = reinterpret_cast<int*>(tmem_holder + 1);
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
@@ -133,20 +142,21 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
   const int g = blockIdx.y;
   const int z = blockIdx.z;
   const int G = p.group;
-  const int TQ = pp.tq;
+  const int TQ = pp.tq;          // tokens of one q tile
+  const int TB = NQ * TQ;        // tokens of the CTA's q-block
 
   // Longest walks first: slots are taken in reverse order.
   const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
-  const int b = pf_find_seq(p.cu_seqlens_q, p.num_seqs, x, TQ);
+  const int b = pf_find_seq(p.cu_seqlens_q, p.num_seqs, x, TB);
   const int q0 = __ldg(p.cu_seqlens_q + b);
   const int q_len = __ldg(p.cu_seqlens_q + b + 1) - q0;
   const int kv_len = __ldg(p.seq_lens_k + b);
-  const int t_first = (x - (q0 / TQ + b)) * TQ;  // first token of the block within the sequence
+  const int t_first = (x - (q0 / TB + b)) * TB;  // first token of the block within the sequence
   if (t_first < 0 || t_first >= q_len) return;   // idle slot: uniform for the CTA
-  const int t_last = min(t_first + TQ, q_len) - 1;
-  const int rows = (t_last - t_first + 1) * G;   // valid rows of the 128
+  const int nq_act = min(NQ, (q_len - t_first + TQ - 1) / TQ);  // q tiles holding tokens
   const int ctx = kv_len - q_len;
-  const int pos_first = ctx + t_first, pos_last = ctx + t_last;
+  // The CTA's key range: the union of its tiles' ranges, split into n_part partitions.
+  const int pos_first = ctx + t_first, pos_last = ctx + min(t_first + TB, q_len) - 1;
   const int hi = max(0, min(pos_last + 1, kv_len));
   const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
   int part = (hi - lo + p.n_part - 1) / p.n_part;
@@ -154,34 +164,51 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
   const int ks = min(lo + z * part, hi);
   const int ke = min(ks + part, hi);
   const int nt = (ke - ks + BN - 1) / BN;
+  // Key tiles [jb, je) of q tile qt: those its own tokens attend to.
+  auto tile_walk = [&](int qt, int& jb, int& je) {
+    jb = je = 0;
+    if (qt >= nq_act) return;
+    const int tf = t_first + qt * TQ, tl = min(tf + TQ, q_len) - 1;
+    const int a = max(ks, p.window_left >= 0 ? max(0, ctx + tf - p.window_left) : 0);
+    const int e = min(ke, max(0, min(ctx + tl + 1, kv_len)));
+    if (a < e) {
+      jb = (a - ks) / BN;
+      je = (e - ks + BN - 1) / BN;
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-      lo_flag[i] = 0;
-    }
+    mbar_init(fin, 1);
     for (int i = 0; i < R; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
-    mbar_init(fin, 1);
+    for (int qt = 0; qt < NQ; ++qt) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(s_full(qt, i), 1);
+        mbar_init(s_free(qt, i), 4);
+        lo_flag[2 * qt + i] = 0;
+      }
+      mbar_init(p_full(qt), 4);
+      mbar_init(pv_done(qt), 1);
+    }
     s_abort = 0;
     mbar_fence_init();
   }
-  // Q rows past the block stay zero (they are computed and dropped).
-  for (int i = threadIdx.x; i < C::kCB * (C::kBM - TQ * G) * 8; i += C::kThreads) {
-    const int cb = i / ((C::kBM - TQ * G) * 8), rem = i % ((C::kBM - TQ * G) * 8);
-    *reinterpret_cast<uint4*>(sQ + cb * C::kBM * 128 + (TQ * G + rem / 8) * 128 + (rem % 8) * 16) =
-        make_uint4(0, 0, 0, 0);
+  // Q rows past the tokens of a tile stay zero (they are computed and dropped).
+  {
+    const int pad = (C::kBM - TQ * G) * 8;  // 16-byte chunks per column block
+    for (int i = threadIdx.x; i < NQ * C::kCB * pad; i += C::kThreads) {
+      const int qc = i / pad, rem = i % pad;
+      *reinterpret_cast<uint4*>(sQ + qc * C::kBM * 128 + (TQ * G + rem / 8) * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
   }
   fence_proxy_async_smem();
-  if (warp == 5) {
+  if (warp == kMma) {
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
@@ -189,19 +216,19 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS[2] = {tmem, tmem + BN};
-  const uint32_t tO = tmem + 2 * BN;
   volatile int* abort_flag = &s_abort;
 
-  if (warp == 4) {
+  if (warp == kProducer) {
     // ======================================================== TMA producer
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
     const int bs = p.block_size;
     const int oob = p.num_blocks * bs;
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, C::kCB * TQ * G * 128);
-      for (int cb = 0; cb < C::kCB; ++cb)
-        tma_load_3d_pf(sQ + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G, q0 + t_first, q_full);
+      mbar_arrive_expect_tx(q_full, nq_act * C::kCB * TQ * G * 128);
+      for (int qt = 0; qt < nq_act; ++qt)
+        for (int cb = 0; cb < C::kCB; ++cb)
+          tma_load_3d_pf(sQ + qt * C::kQBytes + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G,
+                         q0 + t_first + qt * TQ, q_full);
     }
     auto page_row = [&](int j) -> int {
       const int key = ks + j * BN + 16 * lane;
@@ -245,10 +272,15 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
       mbar_wait_bounded(&v_full[j % R], (j / R) & 1, p.status, DEV_TIMEOUT);
     }
     if (lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
-  } else if (warp == 5) {
+  } else if (warp == kMma) {
     // ======================================================== MMA issuer
+    // Per key tile j: S of every q tile (Q_t K_j^T), then O_t += P_t V_{j-1} of every q
+    // tile, so the tensor cores work on one tile while the softmax warps of the other run.
     constexpr uint32_t kIdQK = umma_idesc_f16(128, BN, BF16, false);
     constexpr uint32_t kIdPV = umma_idesc_f16(128, D, BF16, true);
+    int jb[NQ], je[NQ];
+#pragma unroll
+    for (int qt = 0; qt < NQ; ++qt) tile_walk(qt, jb[qt], je[qt]);
     bool ok = pf_wait(q_full, 0, abort_flag, p.status);
     auto do_pv = [&](int i) -> bool {
       const int vs_i = i % R;
@@ -267,46 +299,62 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (!pf_wait(p_full, i & 1, abort_flag, p.status)) return false;
-      tc_fence_after();
-      const bool use_lo = BF16 && lo_flag[i & 1] == i + 1;
-      if (lane == 0) {
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          if (part == 1 && !use_lo) break;
-          const uint32_t pbase = smem_addr(sP + part * C::kPBytes);
+      for (int qt = 0; qt < NQ; ++qt) {
+        if (i < jb[qt] || i >= je[qt]) continue;
+        const int n = i - jb[qt];
+        if (!pf_wait(p_full(qt), n & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const bool use_lo = BF16 && lo_flag[2 * qt + (n & 1)] == n + 1;
+        if (lane == 0) {
+          const uint32_t tO = tmem + qt * C::kTmemStride + 2 * BN;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t ad =
-                smem_desc_sw128(pbase + (kk >> 2) * C::kPCB + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(smem_addr(vs) + kk * 16 * 128, C::kKVCB, 1024);
-            umma_f16_ss(tO, ad, bd, kIdPV, (i > 0 || kk > 0 || part > 0) ? 1u : 0u);
+          for (int part = 0; part < 2; ++part) {
+            if (part == 1 && !use_lo) break;
+            const uint32_t pbase = smem_addr(sP + (2 * qt + part) * C::kPBytes);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t ad =
+                  smem_desc_sw128(pbase + (kk >> 2) * C::kPCB + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(smem_addr(vs) + kk * 16 * 128, C::kKVCB, 1024);
+              umma_f16_ss(tO, ad, bd, kIdPV, (n > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            }
           }
+          umma_commit(pv_done(qt));
         }
-        umma_commit(pv_done);
-        umma_commit(&v_empty[vs_i]);
+        __syncwarp();
       }
+      if (lane == 0) umma_commit(&v_empty[vs_i]);
       __syncwarp();
       return true;
     };
     for (int j = 0; ok && j < nt; ++j) {
       const int ks_j = j % R;
       if (!pf_wait(&k_full[ks_j], (j / R) & 1, abort_flag, p.status)) { ok = false; break; }
-      const int s = j & 1;
-      if (j >= 2 && !pf_wait(&s_free[s], ((j >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t qb = smem_addr(sQ);
-        const uint32_t kb = smem_addr(sK + ks_j * C::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kKVCB + (kk & 3) * 32, 16, 1024);
-          umma_f16_ss(tS[s], ad, bd, kIdQK, kk > 0 ? 1u : 0u);
+      for (int qt = 0; qt < NQ; ++qt) {
+        if (j < jb[qt] || j >= je[qt]) continue;
+        const int n = j - jb[qt], s = n & 1;
+        if (n >= 2 && !pf_wait(s_free(qt, s), ((n >> 1) - 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
         }
-        umma_commit(&s_full[s]);
-        umma_commit(&k_empty[ks_j]);
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t qb = smem_addr(sQ + qt * C::kQBytes);
+          const uint32_t kb = smem_addr(sK + ks_j * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kKVCB + (kk & 3) * 32, 16, 1024);
+            umma_f16_ss(tmem + qt * C::kTmemStride + s * BN, ad, bd, kIdQK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full(qt, s));
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&k_empty[ks_j]);
       __syncwarp();
       if (j >= 1 && !do_pv(j - 1)) { ok = false; break; }
     }
@@ -317,10 +365,16 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
     mbar_wait_bounded(fin, 0, p.status, DEV_TIMEOUT);
   } else {
     // ======================================================== softmax warps (thread = row)
-    const int r = 32 * warp + lane;
-    const int tl = r / G;                                  // token within the block
-    const bool rv = r < rows && q0 + t_first + tl < p.total_q;
-    const int i_q = t_first + (rv ? tl : 0);               // query index within the sequence
+    const int qt = warp >> 2;                              // q tile of this warp
+    const int quad = warp & 3;                             // its tensor-memory lane quarter
+    const int r = 32 * quad + lane;                        // row within the q tile
+    int jb, je;
+    tile_walk(qt, jb, je);
+    const int n_tiles = je - jb;
+    const int tf = t_first + qt * TQ;
+    const int tl = r / G;                                  // token within the q tile
+    const bool rv = qt < nq_act && r < TQ * G && tf + tl < q_len && q0 + tf + tl < p.total_q;
+    const int i_q = tf + (rv ? tl : 0);                    // query index within the sequence
     const int h = g * G + r % G;
     const int pos = ctx + i_q;
     const int lo_r = p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
@@ -343,33 +397,35 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
     const bool sink = p.sinks != nullptr && z == 0 && rv;
     float m_used = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
     float l = sink ? 1.f : 0.f;
-    const uint32_t lane_off = (32u * warp) << 16;
+    const uint32_t lane_off = (32u * quad) << 16;
+    const uint32_t tS0 = tmem + qt * C::kTmemStride + lane_off;
+    const uint32_t tO = tS0 + 2 * BN;
     bool ok = true;
-    uint8_t* const pw_hi = sP + r * 128;
-    uint8_t* const pw_lo = sP + C::kPBytes + r * 128;
+    uint8_t* const pw_hi = sP + (2 * qt) * C::kPBytes + r * 128;
+    uint8_t* const pw_lo = pw_hi + C::kPBytes;
     bool lo_dirty = true;  // the low P rows of this thread hold something other than zeros
 
-    for (int j = 0; j < nt; ++j) {
-      const int s = j & 1;
-      if (!pf_wait(&s_full[s], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+    for (int n = 0; n < n_tiles; ++n) {
+      const int s = n & 1;
+      if (!pf_wait(s_full(qt, s), (n >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       float x[BN];
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t rr[32];
-        tmem_ld32(tS[s] + lane_off + c0, rr);
+        tmem_ld32(tS0 + s * BN + c0, rr);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c0 + e] = __uint_as_float(rr[e]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[s]);
+      if (lane == 0) mbar_arrive(s_free(qt, s));
 
       // ---- scores: with no softcap or bias the log2-domain score is c * s with
       // c = scale * log2(e) > 0, so the row max is taken on the raw dot products and the
       // scale is folded into the exponent's FMA; softcap and biases are applied first
-      const int k0 = ks + j * BN;
+      const int k0 = ks + (jb + n) * BN;
       const bool need_mask = k0 < lomax || k0 + BN - 1 > pmin || k0 + BN > ke;
       float c = scale_log2;
       if constexpr (FEAT) {
@@ -427,27 +483,27 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
       // the low part of P matters only where one key can still weigh more than 1/64
       const bool need_lo = BF16 && pmax * 64.f > l;
 
-      // ---- P buffer free and O final for tile j-1
-      if (j >= 1) {
-        if (!pf_wait(pv_done, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      // ---- P buffer free and O final for step n-1
+      if (n >= 1) {
+        if (!pf_wait(pv_done(qt), (n - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
       }
-      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+      if (n >= 1 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t rr[32];
-          tmem_ld32(tO + lane_off + c0, rr);
+          tmem_ld32(tO + c0, rr);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-          tmem_st32(tO + lane_off + c0, rr);
+          tmem_st32(tO + c0, rr);
         }
         tmem_st_wait();
       }
       // ---- P rows to shared memory (128-byte swizzled, K-major A operand).  The low
       // part is computed only by warps with a row that needs it; a warp that does not
       // keeps zeros in its low rows (written once), so the MMA may use the low buffer
-      // whenever any warp asks for it.
+      // whenever any warp of the tile asks for it.
       const bool warp_lo = BF16 && __any_sync(0xffffffffu, need_lo);
 #pragma unroll
       for (int cq = 0; cq < BN / 8; ++cq) {
@@ -473,15 +529,15 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
         }
       }
       if (BF16) lo_dirty = warp_lo;
-      if (warp_lo && lane == 0) lo_flag[j & 1] = j + 1;
+      if (warp_lo && lane == 0) lo_flag[2 * qt + (n & 1)] = n + 1;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(qt));
     }
 
     // ---- epilogue: O / l for one partition, or the partition's max / sum / O
-    if (ok && nt > 0) ok = pf_wait(pv_done, (nt - 1) & 1, abort_flag, p.status);
+    if (ok && n_tiles > 0) ok = pf_wait(pv_done(qt), (n_tiles - 1) & 1, abort_flag, p.status);
     tc_fence_after();
     if (ok) {
       const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
@@ -490,8 +546,8 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t rr[32];
-        if (nt > 0) {
-          tmem_ld32(tO + lane_off + c0, rr);
+        if (n_tiles > 0) {
+          tmem_ld32(tO + c0, rr);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -537,13 +593,13 @@ __global__ void __launch_bounds__(192, 1) ua_prefill_tc_kernel(const __grid_cons
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D, bool BF16, bool FEAT>
+template <int D, int NQ, bool BF16, bool FEAT>
 cudaError_t launch_prefill_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
-  using C = PrefillCfg<D>;
-  auto kern = ua_prefill_tc_kernel<D, BF16, FEAT>;
+  using C = PrefillCfg<D, NQ>;
+  auto kern = ua_prefill_tc_kernel<D, NQ, BF16, FEAT>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -557,13 +613,26 @@ cudaError_t launch_prefill_t(const PrefillParams& pp, dim3 grid, cudaStream_t st
   return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, 1, pp);
 }
 
-template <int D>
-cudaError_t launch_prefill_dispatch(const PrefillParams& pp, dim3 grid, int kv, bool feat,
-                                    cudaStream_t s) {
+template <int D, int NQ>
+cudaError_t launch_prefill_nq(const PrefillParams& pp, dim3 grid, int kv, bool feat,
+                              cudaStream_t s) {
   if (kv == KV_BF16)
-    return feat ? launch_prefill_t<D, true, true>(pp, grid, s) : launch_prefill_t<D, true, false>(pp, grid, s);
+    return feat ? launch_prefill_t<D, NQ, true, true>(pp, grid, s)
+                : launch_prefill_t<D, NQ, true, false>(pp, grid, s);
   if (kv == KV_F16)
-    return feat ? launch_prefill_t<D, false, true>(pp, grid, s) : launch_prefill_t<D, false, false>(pp, grid, s);
+    return feat ? launch_prefill_t<D, NQ, false, true>(pp, grid, s)
+                : launch_prefill_t<D, NQ, false, false>(pp, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+// nq: q tiles of 128 rows per CTA (1, or 2 where two tiles' tensor memory fits: D <= 128).
+template <int D>
+cudaError_t launch_prefill_dispatch(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
+                                    cudaStream_t s) {
+  if constexpr (prefill_two_tiles_fit(D)) {
+    if (nq == 2) return launch_prefill_nq<D, 2>(pp, grid, kv, feat, s);
+  }
+  if (nq == 1) return launch_prefill_nq<D, 1>(pp, grid, kv, feat, s);
   return cudaErrorInvalidValue;
 }
 

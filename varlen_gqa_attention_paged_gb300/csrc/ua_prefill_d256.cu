@@ -3,9 +3,9 @@
 
 namespace ua {
 
-cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool feat,
+cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
                                 cudaStream_t s) {
-  return launch_prefill_dispatch<256>(pp, grid, kv, feat, s);
+  return launch_prefill_dispatch<256>(pp, grid, kv, feat, nq, s);
 }
 
 }  // namespace ua
