@@ -1,5 +1,8 @@
 // ua_prefill.cuh -- the tensor-memory attention kernel of libua.so for prefill-shaped
-// q-blocks (included by ua_prefill_d*.cu).
+// q-blocks with head_dim 256 (included by ua_prefill_d256.cu), and the helpers it shares
+// with the head_dim <= 128 kernel of ua_prefill_tm.cuh.  At head_dim 256 two 128-key K/V
+// tiles do not fit in shared memory beside Q, so this kernel walks 64-key tiles and keeps P
+// in shared memory, with S double-buffered in tensor memory.
 //
 // One CTA owns (q-block, kv-head g, key partition z).  A q-block is TQ consecutive query
 // tokens of one sequence times the G query heads that read kv-head g, packed as
@@ -88,6 +91,13 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile
     }
   }
   return true;
+}
+
+// pf_wait for a whole warp: every lane waits, and the result is the same in every lane
+// (a lane that gave up makes the warp give up), so the warp stays converged.
+__device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, unsigned int* status) {
+  return __all_sync(0xffffffffu, pf_wait(bar, parity, abort_flag, status));
 }
 
 // Sequence owning token-block slot x: the last b with floor(cu[b] / TQ) + b <= x.

@@ -1,0 +1,568 @@
+// ua_prefill_tm.cuh -- the tensor-memory attention kernel of libua.so for prefill-shaped
+// q-blocks with head_dim <= 128 (included by ua_prefill_d64.cu and ua_prefill_d128.cu).
+//
+// One CTA owns (q-block, kv-head g, key partition z).  A q-block is NQ (1 or 2) q tiles of
+// 128 rows; a tile is TQ = floor(128 / G) consecutive query tokens times the G query heads
+// that read kv-head g, so the GQA heads of a group share every K/V tile (vllm-rdna PR #34
+// "FA-RDNA2 D=128 prefill", "Change" 1, on tensor cores), and the NQ tiles share them too.
+// Per key tile of BN = 128 keys and q tile t:
+//
+//   S_t = Q_t K^T   tcgen05.mma (kind::f16, M=128, N=128, fp32) into tensor memory
+//   softmax         one thread per row: pass 1 reads the S row from tensor memory for the
+//                   row max (after scale, softcap, ALiBi, QQ-bias and the causal/window
+//                   mask); pass 2 reads it again and writes P = 2^(s - m) back over S as
+//                   bf16 high part + remainder (or f16), 32 keys at a time
+//   O_t += P_t V    tcgen05.mma with A = P read from tensor memory and V from shared memory
+//
+// Tensor memory per q tile: S/P (128 columns) and O (D columns); two tiles fill the 512
+// columns at D = 128.  Because P overwrites S, a tile's next S is issued after its P.V;
+// the MMA warp alternates the tiles (P.V then S of tile 0, P.V then S of tile 1) so the
+// tensor cores work on one tile while the other tile's softmax runs.  Each commit tracks
+// every earlier MMA of the issuing thread, so "S of step n is ready" also means "O holds
+// P.V of step n-1": the softmax rescales O (only when a row's max grows by more than 2^8)
+// right after that wait, with no extra barrier.
+//
+// Warp roles (128 * NQ + 64 threads): warps 0..4NQ-1 softmax + epilogue (warp w serves
+// tile w / 4, tensor-memory lanes 32 (w % 4) ..; thread = row), warp 4NQ TMA producer (Q
+// once, then K and V pages of 16 keys through the block table into two rings, 128-byte
+// swizzled), warp 4NQ+1 MMA issuer and tensor-memory owner.
+#pragma once
+
+#include <atomic>
+#include <climits>
+#include <type_traits>
+
+#include <cuda.h>
+
+#include "ua_device.cuh"
+#include "ua_internal.h"
+#include "ua_prefill.cuh"
+
+#include "ua.h"
+
+namespace ua {
+
+template <int D, int NQ>
+struct PrefillTmCfg {
+  static constexpr int kBM = 128;                        // MMA rows of one q tile
+  static constexpr int kBN = 128;                        // keys per tile
+  static constexpr int kCB = D / 64;                     // 128-byte column blocks of a row
+  static constexpr int kQBytes = kCB * kBM * 128;        // one q tile
+  static constexpr int kKVCB = kBN * 128;                // one column block of a K or V tile
+  static constexpr int kTileBytes = kCB * kKVCB;         // one K (or V) tile
+  static constexpr int kBarBytes = 512;
+  // K and V ring depths: as many tiles as fit beside Q (K gets the odd one, at most 4 each)
+  static constexpr int kSlots = (227 * 1024 - 1024 - kBarBytes - NQ * kQBytes) / kTileBytes;
+  static constexpr int kRingK = (kSlots + 1) / 2 > 4 ? 4 : (kSlots + 1) / 2;
+  static constexpr int kRingV = kSlots / 2 > 4 ? 4 : kSlots / 2;
+  static constexpr int kSmemBytes =
+      1024 + NQ * kQBytes + (kRingK + kRingV) * kTileBytes + kBarBytes;
+  static constexpr int kTmemStride = kBN + D;            // S/P, then O, of one q tile
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSoftmaxWarps = 4 * NQ;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 64;
+  static_assert(D <= 128, "two 128-key K/V rings must fit");
+  static_assert(NQ * kTmemStride <= kTmemCols, "tensor memory budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kRingK >= 2 && kRingV >= 2, "at least double-buffered K and V");
+};
+
+template <int D, int NQ, bool BF16, bool FEAT>
+__global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
+    ua_prefill_tm_kernel(const __grid_constant__ PrefillParams pp) {
+  using C = PrefillTmCfg<D, NQ>;
+  constexpr int BN = C::kBN;
+  constexpr int RK = C::kRingK, RV = C::kRingV;
+  constexpr int kProducer = C::kSoftmaxWarps, kMma = C::kSoftmaxWarps + 1;
+  const AttnParams& p = pp.p;
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* const smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* const sQ = smem;                          // NQ q tiles
+  uint8_t* const sK = sQ + NQ * C::kQBytes;          // RK K tiles
+  uint8_t* const sV = sK + RK * C::kTileBytes;       // RV V tiles
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(sV + RV * C::kTileBytes);
+  uint64_t* const q_full = bars + 0;
+  uint64_t* const fin = bars + 1;
+  uint64_t* const k_full = bars + 2;                 // [RK]
+  uint64_t* const k_empty = k_full + RK;             // [RK]
+  uint64_t* const v_full = k_empty + RK;             // [RV]
+  uint64_t* const v_empty = v_full + RV;             // [RV]
+  uint64_t* const tile_bars = v_empty + RV;          // [NQ][3]: s_full, p_full, pv_done
+  auto s_full = [&](int qt) { return tile_bars + 3 * qt; };
+  auto p_full = [&](int qt) { return tile_bars + 3 * qt + 1; };
+  auto pv_done = [&](int qt) { return tile_bars + 3 * qt + 2; };
+  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(tile_bars + 3 * NQ);
+  // [NQ][2]: walk step + 1 of the tile's P when its low part matters
+  int* const lo_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.y;
+  const int z = blockIdx.z;
+  const int G = p.group;
+  const int TQ = pp.tq;          // tokens of one q tile
+  const int TB = NQ * TQ;        // tokens of the CTA's q-block
+
+  // Longest walks first: slots are taken in reverse order.
+  const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  const int b = pf_find_seq(p.cu_seqlens_q, p.num_seqs, x, TB);
+  const int q0 = __ldg(p.cu_seqlens_q + b);
+  const int q_len = __ldg(p.cu_seqlens_q + b + 1) - q0;
+  const int kv_len = __ldg(p.seq_lens_k + b);
+  const int t_first = (x - (q0 / TB + b)) * TB;  // first token of the block within the sequence
+  if (t_first < 0 || t_first >= q_len) return;   // idle slot: uniform for the CTA
+  const int nq_act = min(NQ, (q_len - t_first + TQ - 1) / TQ);  // q tiles holding tokens
+  const int ctx = kv_len - q_len;
+  // The CTA's key range: the union of its tiles' ranges, split into n_part partitions.
+  const int pos_first = ctx + t_first, pos_last = ctx + min(t_first + TB, q_len) - 1;
+  const int hi = max(0, min(pos_last + 1, kv_len));
+  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
+  int part = (hi - lo + p.n_part - 1) / p.n_part;
+  part = (part + 15) & ~15;
+  const int ks = min(lo + z * part, hi);
+  const int ke = min(ks + part, hi);
+  const int nt = (ke - ks + BN - 1) / BN;
+  // Key tiles [jb, je) of q tile qt: those its own tokens attend to.
+  auto tile_walk = [&](int qt, int& jb, int& je) {
+    jb = je = 0;
+    if (qt >= nq_act) return;
+    const int tf = t_first + qt * TQ, tl = min(tf + TQ, q_len) - 1;
+    const int a = max(ks, p.window_left >= 0 ? max(0, ctx + tf - p.window_left) : 0);
+    const int e = min(ke, max(0, min(ctx + tl + 1, kv_len)));
+    if (a < e) {
+      jb = (a - ks) / BN;
+      je = (e - ks + BN - 1) / BN;
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(fin, 1);
+    for (int i = 0; i < RK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < RV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int qt = 0; qt < NQ; ++qt) {
+      mbar_init(s_full(qt), 1);
+      mbar_init(p_full(qt), 4);
+      mbar_init(pv_done(qt), 1);
+      lo_flag[2 * qt] = lo_flag[2 * qt + 1] = 0;
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  // Q rows past the tokens of a tile stay zero (they are computed and dropped).
+  {
+    const int pad = (C::kBM - TQ * G) * 8;  // 16-byte chunks per column block
+    for (int i = threadIdx.x; i < NQ * C::kCB * pad; i += C::kThreads) {
+      const int qc = i / pad, rem = i % pad;
+      *reinterpret_cast<uint4*>(sQ + qc * C::kBM * 128 + (TQ * G + rem / 8) * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+  }
+  fence_proxy_async_smem();
+  if (warp == kMma) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == kProducer) {
+    // ======================================================== TMA producer
+    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    const int bs = p.block_size;
+    const int oob = p.num_blocks * bs;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, nq_act * C::kCB * TQ * G * 128);
+      for (int qt = 0; qt < nq_act; ++qt)
+        for (int cb = 0; cb < C::kCB; ++cb)
+          tma_load_3d_pf(sQ + qt * C::kQBytes + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G,
+                         q0 + t_first + qt * TQ, q_full);
+    }
+    // cache row of this lane's 16-key page of key tile j (lanes 0 .. BN/16-1)
+    auto page_row = [&](int j) -> int {
+      const int key = ks + j * BN + 16 * lane;
+      if (lane >= BN / 16 || key >= ke) return oob;
+      const int col = key / bs;
+      const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+      if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+        atomicOr(p.status, DEV_BAD_BLOCK);
+        return oob;
+      }
+      return blk * bs + key % bs;
+    };
+    int row_next = nt > 0 ? page_row(0) : oob;
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < nt; ++j) {
+      const int row = row_next;
+      if (j + 1 < nt) row_next = page_row(j + 1);
+      const int sk = j % RK, sv = j % RV;
+      if (j >= RK && !pf_wait_warp(&k_empty[sk], ((j / RK) - 1) & 1, abort_flag, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
+      __syncwarp();
+      if (lane < BN / 16)
+#pragma unroll
+        for (int cb = 0; cb < C::kCB; ++cb)
+          tma_load_3d_pf(sK + sk * C::kTileBytes + cb * C::kKVCB + lane * 2048, &pp.tmap_k,
+                         64 * cb, g, row, &k_full[sk]);
+      k_issued = j + 1;
+      if (j >= RV && !pf_wait_warp(&v_empty[sv], ((j / RV) - 1) & 1, abort_flag, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
+      __syncwarp();
+      if (lane < BN / 16)
+#pragma unroll
+        for (int cb = 0; cb < C::kCB; ++cb)
+          tma_load_3d_pf(sV + sv * C::kTileBytes + cb * C::kKVCB + lane * 2048, &pp.tmap_v,
+                         64 * cb, g, row, &v_full[sv]);
+      v_issued = j + 1;
+    }
+    // never leave copies in flight into this CTA's shared memory (even after an abort)
+    for (int j = max(0, k_issued - RK); j < k_issued; ++j)
+      mbar_wait_bounded(&k_full[j % RK], (j / RK) & 1, p.status, DEV_TIMEOUT);
+    for (int j = max(0, v_issued - RV); j < v_issued; ++j)
+      mbar_wait_bounded(&v_full[j % RV], (j / RV) & 1, p.status, DEV_TIMEOUT);
+    if (lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
+  } else if (warp == kMma) {
+    // ======================================================== MMA issuer
+    // Step j: for each q tile, O += P V_{j-1} (which frees the tile's S/P columns), then
+    // S = Q K_j^T.  Tensor-core operations of one thread run in issue order.  The whole
+    // warp runs this loop converged; one elected lane issues each MMA and commit.
+    constexpr uint32_t kIdQK = umma_idesc_f16(128, BN, BF16, false);
+    constexpr uint32_t kIdPV = umma_idesc_f16(128, D, BF16, true);
+    int jb[NQ], je[NQ];
+#pragma unroll
+    for (int qt = 0; qt < NQ; ++qt) tile_walk(qt, jb[qt], je[qt]);
+    bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
+    for (int j = 0; ok && j <= nt; ++j) {
+      const int i = j - 1;  // key tile of this step's P.V
+      uint8_t* vs = sV + (i >= 0 ? i % RV : 0) * C::kTileBytes;
+      if (i >= 0) {
+        if (!pf_wait_warp(&v_full[i % RV], (i / RV) & 1, abort_flag, p.status)) { ok = false; break; }
+        // Cache slots at or past kv_len hold no key and may hold anything (NaN included):
+        // zero those V rows before the tensor cores multiply them by P = 0.
+        const int k0 = ks + i * BN;
+        if (k0 + BN > kv_len) {
+          const int r_lo = max(0, kv_len - k0), r_hi = min(BN, ((kv_len + 15) & ~15) - k0);
+          for (int e = lane; e < (r_hi - r_lo) * C::kCB * 8; e += 32) {
+            const int r = r_lo + e / (C::kCB * 8), c = e % (C::kCB * 8);
+            *reinterpret_cast<uint4*>(vs + (c / 8) * C::kKVCB + r * 128 + (c % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+      }
+      if (j < nt && !pf_wait_warp(&k_full[j % RK], (j / RK) & 1, abort_flag, p.status)) { ok = false; break; }
+#pragma unroll
+      for (int qt = 0; qt < NQ; ++qt) {
+        if (i >= jb[qt] && i < je[qt]) {
+          const int n = i - jb[qt];
+          if (!pf_wait_warp(p_full(qt), n & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const bool use_lo = BF16 && lo_flag[2 * qt + (n & 1)] == n + 1;
+          const uint32_t tP = tmem + qt * C::kTmemStride;
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            if (part == 1 && !use_lo) break;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t bd = smem_desc_sw128(smem_addr(vs) + kk * 16 * 128, C::kKVCB, 1024);
+              umma_f16_ts_warp(tP + BN, tP + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bd, kIdPV,
+                               (n > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            }
+          }
+          if (i == je[qt] - 1) umma_commit_warp(pv_done(qt));
+        }
+        if (j >= jb[qt] && j < je[qt]) {
+          tc_fence_after();
+          const uint32_t qb = smem_addr(sQ + qt * C::kQBytes);
+          const uint32_t kb = smem_addr(sK + (j % RK) * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kKVCB + (kk & 3) * 32, 16, 1024);
+            umma_f16_ss_warp(tmem + qt * C::kTmemStride, ad, bd, kIdQK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit_warp(s_full(qt));
+        }
+      }
+      if (!ok) break;
+      if (j < nt) umma_commit_warp(&k_empty[j % RK]);
+      if (i >= 0) umma_commit_warp(&v_empty[i % RV]);
+    }
+    // nothing may still be in flight on the tensor cores when the memory is freed
+    umma_commit_warp(fin);
+    mbar_wait_bounded(fin, 0, p.status, DEV_TIMEOUT);
+  } else {
+    // ======================================================== softmax warps (thread = row)
+    const int qt = warp >> 2;                              // q tile of this warp
+    const int quad = warp & 3;                             // its tensor-memory lane quarter
+    const int r = 32 * quad + lane;                        // row within the q tile
+    int jb, je;
+    tile_walk(qt, jb, je);
+    const int n_tiles = je - jb;
+    const int tf = t_first + qt * TQ;
+    const int tl = r / G;                                  // token within the q tile
+    const bool rv = qt < nq_act && r < TQ * G && tf + tl < q_len && q0 + tf + tl < p.total_q;
+    const int i_q = tf + (rv ? tl : 0);                    // query index within the sequence
+    const int h = g * G + r % G;
+    const int pos = ctx + i_q;
+    const int lo_r = p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
+    // warp-uniform bounds of this warp's valid rows, to mask only boundary tiles
+    int pmin = rv ? pos : INT_MAX, lomax = rv ? lo_r : INT_MIN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
+      lomax = max(lomax, __shfl_xor_sync(0xffffffffu, lomax, o));
+    }
+    const float inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+    float slope = 0.f;
+    const float* qq_row = nullptr;
+    if constexpr (FEAT) {
+      if (p.alibi != nullptr && rv) slope = __ldg(p.alibi + h);
+      if (p.qq_bias != nullptr && rv && i_q < p.max_seqlen_q)
+        qq_row = p.qq_bias + static_cast<size_t>(i_q) * p.qq_stride;
+    }
+    // With no softcap or bias the log2-domain score is c * s with c = scale * log2(e) > 0:
+    // the row max is taken on the raw dot products and the scale folds into the exponent's
+    // FMA.  Otherwise scores are transformed first and c = log2(e).
+    const float c = FEAT ? kLog2e : p.scale * kLog2e;
+    const bool sink = p.sinks != nullptr && z == 0 && rv;
+    float m_used = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+    float l = sink ? 1.f : 0.f;
+    const uint32_t tS = tmem + qt * C::kTmemStride + ((32u * quad) << 16);
+    const uint32_t tO = tS + BN;
+    bool ok = true;
+
+    // softcap / ALiBi / QQ-bias, then (MASK: a boundary tile) the causal / window /
+    // partition mask
+    auto score = [&](float v, int jk, auto mask) -> float {
+      if constexpr (FEAT) {
+        v *= p.scale;
+        if (p.softcap > 0.f) v = p.softcap * tanhf(v * inv_softcap);
+        v += slope * static_cast<float>(jk - ctx);
+        if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
+      }
+      if constexpr (decltype(mask)::value) {
+        if (!(rv && jk >= lo_r && jk <= pos && jk < ke)) v = -INFINITY;
+      }
+      return v;
+    };
+
+    for (int n = 0; n < n_tiles; ++n) {
+      if (!pf_wait_warp(s_full(qt), n & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const int k0 = ks + (jb + n) * BN;
+      const bool need_mask = k0 < lomax || k0 + BN - 1 > pmin || k0 + BN > ke;
+
+      // ---- pass 1: row max (two 32-column loads in flight)
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tS + c0, ra);
+        tmem_ld32(tS + c0 + 32, rb);
+        tmem_ld_wait();
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            mx0 = fmaxf(mx0, score(__uint_as_float(ra[e]), k0 + c0 + e, std::true_type{}));
+            mx1 = fmaxf(mx1, score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::true_type{}));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            mx0 = fmaxf(mx0, score(__uint_as_float(ra[e]), k0 + c0 + e, std::false_type{}));
+            mx1 = fmaxf(mx1, score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::false_type{}));
+          }
+        }
+      }
+      const float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
+      // ---- running max, used lazily: O and l are rescaled only when the max grows by
+      // more than 8 in log2 units (P stays <= 256, far inside the fp32 and P ranges)
+      float alpha = 1.f;
+      const bool grow = mx > m_used + 8.f || (m_used == -INFINITY && mx > -INFINITY);
+      if (grow) {
+        alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mx);
+        m_used = mx;
+      }
+      const float m_use = m_used == -INFINITY ? 0.f : m_used;
+      // O holds P.V of step n-1 (its commit preceded this step's S): rescale it in place
+      if (n >= 1 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tO + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st32(tO + c0, rr);
+        }
+      }
+      // the low part of P matters only where one key can still weigh more than 1/64 of the
+      // row sum; l * alpha + pmax is a lower bound of the new sum
+      const float pmax = mx == -INFINITY ? 0.f : fast_exp2(mx - m_use);
+      const bool warp_lo = BF16 && __any_sync(0xffffffffu, pmax * 63.f > l * alpha);
+
+      // ---- pass 2: P = 2^(c s - m) over S, 32 keys at a time: 16 columns of high part
+      // (bf16 or f16 pairs), then 16 columns of bf16 remainder (zeros when not needed)
+      const float2 cc = make_float2(c, c), mm = make_float2(-m_use, -m_use);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tS + c0, rr);
+        tmem_ld_wait();
+        float xv[32];
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xv[e] = score(__uint_as_float(rr[e]), k0 + c0 + e, std::true_type{});
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xv[e] = score(__uint_as_float(rr[e]), k0 + c0 + e, std::false_type{});
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float2 u = __ffma2_rn(make_float2(xv[e], xv[e + 1]), cc, mm);
+          const float2 w = __ffma2_rn(make_float2(xv[e + 2], xv[e + 3]), cc, mm);
+          xv[e] = fast_exp2(u.x);
+          xv[e + 1] = fast_exp2(u.y);
+          xv[e + 2] = fast_exp2(w.x);
+          xv[e + 3] = fast_exp2(w.y);
+          acc0 = __fadd2_rn(acc0, make_float2(xv[e], xv[e + 1]));
+          acc1 = __fadd2_rn(acc1, make_float2(xv[e + 2], xv[e + 3]));
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t hw = BF16 ? pack_bf16(xv[2 * e], xv[2 * e + 1]) : pack_f16(xv[2 * e], xv[2 * e + 1]);
+          rr[e] = hw;
+          if (BF16 && warp_lo) {
+            const float2 rem = __fadd2_rn(make_float2(xv[2 * e], xv[2 * e + 1]),
+                                          make_float2(-bf16_lo(hw), -bf16_hi(hw)));
+            rr[16 + e] = pack_bf16(rem.x, rem.y);
+          } else {
+            rr[16 + e] = 0u;
+          }
+        }
+        tmem_st32(tS + c0, rr);
+      }
+      l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+      tmem_st_wait();
+      if (warp_lo && lane == 0) lo_flag[2 * qt + (n & 1)] = n + 1;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(qt));
+    }
+
+    // ---- epilogue: O / l for one partition, or the partition's max / sum / O
+    if (ok && n_tiles > 0) ok = pf_wait_warp(pv_done(qt), 0, abort_flag, p.status);
+    tc_fence_after();
+    if (ok) {
+      const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
+      const size_t n_part = static_cast<size_t>(p.n_part);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t rr[32];
+        if (n_tiles > 0) {
+          tmem_ld32(tO + c0, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = 0u;
+        }
+        if (!rv) continue;
+        if (n_part == 1) {
+          if (p.out_dtype == UA_DT_F32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + c0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(rr[4 * e]) * inv, __uint_as_float(rr[4 * e + 1]) * inv,
+                                   __uint_as_float(rr[4 * e + 2]) * inv, __uint_as_float(rr[4 * e + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * D + c0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint32_t w[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float a0 = __uint_as_float(rr[8 * e + 2 * q]) * inv;
+                const float a1 = __uint_as_float(rr[8 * e + 2 * q + 1]) * inv;
+                w[q] = p.out_dtype == UA_DT_BF16 ? pack_bf16(a0, a1) : pack_f16(a0, a1);
+              }
+              dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else {
+          const size_t w = orow * n_part + z;
+          if (c0 == 0) {
+            p.ws_m[w] = m_used;
+            p.ws_l[w] = l;
+          }
+          float4* dst = reinterpret_cast<float4*>(p.ws_acc + w * D + c0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
+                                 __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D, int NQ, bool BF16, bool FEAT>
+cudaError_t launch_prefill_tm_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
+  using C = PrefillTmCfg<D, NQ>;
+  auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT>;
+  static std::atomic<unsigned long long> configured{0};  // one bit per device
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    configured.fetch_or(bit);
+  }
+  return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, 1, pp);
+}
+
+template <int D, int NQ>
+cudaError_t launch_prefill_tm_nq(const PrefillParams& pp, dim3 grid, int kv, bool feat,
+                                 cudaStream_t s) {
+  if (kv == KV_BF16)
+    return feat ? launch_prefill_tm_t<D, NQ, true, true>(pp, grid, s)
+                : launch_prefill_tm_t<D, NQ, true, false>(pp, grid, s);
+  if (kv == KV_F16)
+    return feat ? launch_prefill_tm_t<D, NQ, false, true>(pp, grid, s)
+                : launch_prefill_tm_t<D, NQ, false, false>(pp, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+// nq: q tiles of 128 rows per CTA (1 or 2).
+template <int D>
+cudaError_t launch_prefill_tm_dispatch(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
+                                       cudaStream_t s) {
+  if (nq == 2) return launch_prefill_tm_nq<D, 2>(pp, grid, kv, feat, s);
+  if (nq == 1) return launch_prefill_tm_nq<D, 1>(pp, grid, kv, feat, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ua
