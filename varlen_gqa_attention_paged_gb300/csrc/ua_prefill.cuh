@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
       const uint32_t ph = ((j / R) - 1) & 1;  // phase of the release of tile j - R
       const int row = row_next;
       if (j + 1 < nt) row_next = page_row(j + 1);
-      if (j >= R && !pf_wait(&k_empty[s], ph, abort_flag, p.status)) break;
+      if (j >= R && !pf_wait_warp(&k_empty[s], ph, abort_flag, p.status)) break;
       if (lane == 0) mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
       __syncwarp();
       if (lane < BN / 16)
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
         for (int cb = 0; cb < C::kCB; ++cb)
           tma_load_3d_pf(sK + s * C::kTileBytes + cb * C::kKVCB + lane * 2048, &pp.tmap_k,
                          64 * cb, g, row, &k_full[s]);
-      if (j >= R && !pf_wait(&v_empty[s], ph, abort_flag, p.status)) break;
+      if (j >= R && !pf_wait_warp(&v_empty[s], ph, abort_flag, p.status)) break;
       if (lane == 0) mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
       __syncwarp();
       if (lane < BN / 16)
@@ -286,15 +286,16 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
     // ======================================================== MMA issuer
     // Per key tile j: S of every q tile (Q_t K_j^T), then O_t += P_t V_{j-1} of every q
     // tile, so the tensor cores work on one tile while the softmax warps of the other run.
+    // The whole warp runs this converged; one elected lane issues each MMA and commit.
     constexpr uint32_t kIdQK = umma_idesc_f16(128, BN, BF16, false);
     constexpr uint32_t kIdPV = umma_idesc_f16(128, D, BF16, true);
     int jb[NQ], je[NQ];
 #pragma unroll
     for (int qt = 0; qt < NQ; ++qt) tile_walk(qt, jb[qt], je[qt]);
-    bool ok = pf_wait(q_full, 0, abort_flag, p.status);
+    bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
     auto do_pv = [&](int i) -> bool {
       const int vs_i = i % R;
-      if (!pf_wait(&v_full[vs_i], (i / R) & 1, abort_flag, p.status)) return false;
+      if (!pf_wait_warp(&v_full[vs_i], (i / R) & 1, abort_flag, p.status)) return false;
       uint8_t* vs = sV + vs_i * C::kTileBytes;
       // Cache slots at or past kv_len hold no key and may hold anything (NaN included):
       // zero those V rows before the tensor cores multiply them by P = 0.
@@ -313,65 +314,56 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
       for (int qt = 0; qt < NQ; ++qt) {
         if (i < jb[qt] || i >= je[qt]) continue;
         const int n = i - jb[qt];
-        if (!pf_wait(p_full(qt), n & 1, abort_flag, p.status)) return false;
+        if (!pf_wait_warp(p_full(qt), n & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const bool use_lo = BF16 && lo_flag[2 * qt + (n & 1)] == n + 1;
-        if (lane == 0) {
-          const uint32_t tO = tmem + qt * C::kTmemStride + 2 * BN;
+        const uint32_t tO = tmem + qt * C::kTmemStride + 2 * BN;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            if (part == 1 && !use_lo) break;
-            const uint32_t pbase = smem_addr(sP + (2 * qt + part) * C::kPBytes);
+        for (int part = 0; part < 2; ++part) {
+          if (part == 1 && !use_lo) break;
+          const uint32_t pbase = smem_addr(sP + (2 * qt + part) * C::kPBytes);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t ad =
-                  smem_desc_sw128(pbase + (kk >> 2) * C::kPCB + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(smem_addr(vs) + kk * 16 * 128, C::kKVCB, 1024);
-              umma_f16_ss(tO, ad, bd, kIdPV, (n > 0 || kk > 0 || part > 0) ? 1u : 0u);
-            }
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t ad =
+                smem_desc_sw128(pbase + (kk >> 2) * C::kPCB + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(smem_addr(vs) + kk * 16 * 128, C::kKVCB, 1024);
+            umma_f16_ss_warp(tO, ad, bd, kIdPV, (n > 0 || kk > 0 || part > 0) ? 1u : 0u);
           }
-          umma_commit(pv_done(qt));
         }
-        __syncwarp();
+        umma_commit_warp(pv_done(qt));
       }
-      if (lane == 0) umma_commit(&v_empty[vs_i]);
-      __syncwarp();
+      umma_commit_warp(&v_empty[vs_i]);
       return true;
     };
     for (int j = 0; ok && j < nt; ++j) {
       const int ks_j = j % R;
-      if (!pf_wait(&k_full[ks_j], (j / R) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!pf_wait_warp(&k_full[ks_j], (j / R) & 1, abort_flag, p.status)) { ok = false; break; }
 #pragma unroll
       for (int qt = 0; qt < NQ; ++qt) {
         if (j < jb[qt] || j >= je[qt]) continue;
         const int n = j - jb[qt], s = n & 1;
-        if (n >= 2 && !pf_wait(s_free(qt, s), ((n >> 1) - 1) & 1, abort_flag, p.status)) {
+        if (n >= 2 && !pf_wait_warp(s_free(qt, s), ((n >> 1) - 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t qb = smem_addr(sQ + qt * C::kQBytes);
-          const uint32_t kb = smem_addr(sK + ks_j * C::kTileBytes);
+        const uint32_t qb = smem_addr(sQ + qt * C::kQBytes);
+        const uint32_t kb = smem_addr(sK + ks_j * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kKVCB + (kk & 3) * 32, 16, 1024);
-            umma_f16_ss(tmem + qt * C::kTmemStride + s * BN, ad, bd, kIdQK, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full(qt, s));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kKVCB + (kk & 3) * 32, 16, 1024);
+          umma_f16_ss_warp(tmem + qt * C::kTmemStride + s * BN, ad, bd, kIdQK, kk > 0 ? 1u : 0u);
         }
-        __syncwarp();
+        umma_commit_warp(s_full(qt, s));
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&k_empty[ks_j]);
-      __syncwarp();
+      umma_commit_warp(&k_empty[ks_j]);
       if (j >= 1 && !do_pv(j - 1)) { ok = false; break; }
     }
     if (ok && nt > 0) do_pv(nt - 1);
     // nothing may still be in flight on the tensor cores when the memory is freed
-    if (lane == 0) umma_commit(fin);
-    __syncwarp();
+    umma_commit_warp(fin);
     mbar_wait_bounded(fin, 0, p.status, DEV_TIMEOUT);
   } else {
     // ======================================================== softmax warps (thread = row)
@@ -417,7 +409,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
 
     for (int n = 0; n < n_tiles; ++n) {
       const int s = n & 1;
-      if (!pf_wait(s_full(qt, s), (n >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!pf_wait_warp(s_full(qt, s), (n >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       float x[BN];
 #pragma unroll
@@ -495,7 +487,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
 
       // ---- P buffer free and O final for step n-1
       if (n >= 1) {
-        if (!pf_wait(pv_done(qt), (n - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!pf_wait_warp(pv_done(qt), (n - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
       }
       if (n >= 1 && __any_sync(0xffffffffu, grow)) {
@@ -547,7 +539,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
     }
 
     // ---- epilogue: O / l for one partition, or the partition's max / sum / O
-    if (ok && n_tiles > 0) ok = pf_wait(pv_done(qt), (n_tiles - 1) & 1, abort_flag, p.status);
+    if (ok && n_tiles > 0) ok = pf_wait_warp(pv_done(qt), (n_tiles - 1) & 1, abort_flag, p.status);
     tc_fence_after();
     if (ok) {
       const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
