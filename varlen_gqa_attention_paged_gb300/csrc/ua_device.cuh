@@ -320,6 +320,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// tanh(y) = 1 - 2 / (e^(2y) + 1): one ex2 and one approximate divide.  |y| is clamped at
+// 15, where tanh is +-1 to fp32 precision; the absolute error is a few 1e-7.
+__device__ __forceinline__ float fast_tanh(float y) {
+  y = fminf(fmaxf(y, -15.f), 15.f);
+  const float e = fast_exp2(y * 2.8853900817779268f);  // 2 log2(e)
+  return 1.f - __fdividef(2.f, e + 1.f);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

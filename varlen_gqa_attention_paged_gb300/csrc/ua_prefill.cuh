@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, NQ>::kThreads, 1)
         for (int e = 0; e < BN; ++e) {
           const int jk = k0 + e;
           float v = x[e] * p.scale;
-          if (p.softcap > 0.f) v = p.softcap * tanhf(v * inv_softcap);
+          if (p.softcap > 0.f) v = p.softcap * fast_tanh(v * inv_softcap);
           v += slope * static_cast<float>(jk - ctx);
           if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
           x[e] = v;

@@ -9,9 +9,10 @@
 //
 //   S_t = Q_t K^T   tcgen05.mma (kind::f16, M=128, N=128, fp32) into tensor memory
 //   softmax         one thread per row: pass 1 reads the S row from tensor memory for the
-//                   row max (after scale, softcap, ALiBi, QQ-bias and the causal/window
-//                   mask); pass 2 reads it again and writes P = 2^(s - m) back over S as
-//                   bf16 high part + remainder (or f16), 32 keys at a time
+//                   row max (applying scale, softcap, ALiBi, QQ-bias and the causal/window
+//                   mask where a tile needs them, and writing those scores back); pass 2
+//                   reads it again and writes P = 2^(s - m) back over S as bf16 high part
+//                   + remainder (or f16), 32 keys at a time
 //   O_t += P_t V    tcgen05.mma with A = P read from tensor memory and V from shared memory
 //
 // Tensor memory per q tile: S/P (128 columns) and O (D columns); two tiles fill the 512
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     auto score = [&](float v, int jk, auto mask) -> float {
       if constexpr (FEAT) {
         v *= p.scale;
-        if (p.softcap > 0.f) v = p.softcap * tanhf(v * inv_softcap);
+        if (p.softcap > 0.f) v = p.softcap * fast_tanh(v * inv_softcap);
         v += slope * static_cast<float>(jk - ctx);
         if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
       }
@@ -368,7 +369,9 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
       const int k0 = ks + (jb + n) * BN;
       const bool need_mask = k0 < lomax || k0 + BN - 1 > pmin || k0 + BN > ke;
 
-      // ---- pass 1: row max (two 32-column loads in flight)
+      // ---- pass 1: row max (two 32-column loads in flight).  Scores that need a transform
+      // or a mask get it here, once, and are written back over S for pass 2.
+      const bool rewrite = FEAT || need_mask;
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 64) {
@@ -376,20 +379,30 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
         tmem_ld32(tS + c0, ra);
         tmem_ld32(tS + c0 + 32, rb);
         tmem_ld_wait();
-        if (need_mask) {
+        if (rewrite) {
+          if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            mx0 = fmaxf(mx0, score(__uint_as_float(ra[e]), k0 + c0 + e, std::true_type{}));
-            mx1 = fmaxf(mx1, score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::true_type{}));
-          }
-        } else {
+            for (int e = 0; e < 32; ++e) {
+              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, std::true_type{}));
+              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::true_type{}));
+            }
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            mx0 = fmaxf(mx0, score(__uint_as_float(ra[e]), k0 + c0 + e, std::false_type{}));
-            mx1 = fmaxf(mx1, score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::false_type{}));
+            for (int e = 0; e < 32; ++e) {
+              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, std::false_type{}));
+              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::false_type{}));
+            }
           }
+          tmem_st32(tS + c0, ra);
+          tmem_st32(tS + c0 + 32, rb);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          mx0 = fmaxf(mx0, __uint_as_float(ra[e]));
+          mx1 = fmaxf(mx1, __uint_as_float(rb[e]));
         }
       }
+      if (rewrite) tmem_st_wait();
       const float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
       // ---- running max, used lazily: O and l are rescaled only when the max grows by
       // more than 8 in log2 units (P stays <= 256, far inside the fp32 and P ranges)
@@ -427,13 +440,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
         tmem_ld32(tS + c0, rr);
         tmem_ld_wait();
         float xv[32];
-        if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) xv[e] = score(__uint_as_float(rr[e]), k0 + c0 + e, std::true_type{});
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) xv[e] = score(__uint_as_float(rr[e]), k0 + c0 + e, std::false_type{});
-        }
+        for (int e = 0; e < 32; ++e) xv[e] = __uint_as_float(rr[e]);
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const float2 u = __ffma2_rn(make_float2(xv[e], xv[e + 1]), cc, mm);

@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
           float x;
           if constexpr (FEAT) {
             x = sc[n][e] * scale;
-            if (p.softcap > 0.f) x = p.softcap * tanhf(x * inv_softcap);
+            if (p.softcap > 0.f) x = p.softcap * fast_tanh(x * inv_softcap);
             x += slope[rr] * static_cast<float>(j - ctx);
             if (p.qq_bias != nullptr && rv[rr] && j >= ctx && j <= rpos[rr] &&
                 ri[rr] < p.max_seqlen_q)
