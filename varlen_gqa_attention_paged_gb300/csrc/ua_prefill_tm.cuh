@@ -23,10 +23,11 @@
 // P.V of step n-1": the softmax rescales O (only when a row's max grows by more than 2^8)
 // right after that wait, with no extra barrier.
 //
-// Warp roles (128 * NQ + 64 threads): warps 0..4NQ-1 softmax + epilogue (warp w serves
-// tile w / 4, tensor-memory lanes 32 (w % 4) ..; thread = row), warp 4NQ TMA producer (Q
-// once, then K and V pages of 16 keys through the block table into two rings, 128-byte
-// swizzled), warp 4NQ+1 MMA issuer and tensor-memory owner.
+// Warp roles (128 * NQ + 96 threads): warps 0..4NQ-1 softmax + epilogue (warp w serves
+// tile w / 4, tensor-memory lanes 32 (w % 4) ..; thread = row), warps 4NQ and 4NQ+1 TMA
+// producers (Q once and K pages; V pages; pages of 16 keys found through the block table,
+// each operand in its own ring, 128-byte swizzled), warp 4NQ+2 MMA issuer and
+// tensor-memory owner.
 #pragma once
 
 #include <atomic>
@@ -61,7 +62,7 @@ struct PrefillTmCfg {
   static constexpr int kTmemStride = kBN + D;            // S/P, then O, of one q tile
   static constexpr int kTmemCols = 512;
   static constexpr int kSoftmaxWarps = 4 * NQ;
-  static constexpr int kThreads = 32 * kSoftmaxWarps + 64;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 96;
   static_assert(D <= 128, "two 128-key K/V rings must fit");
   static_assert(NQ * kTmemStride <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -74,7 +75,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
   using C = PrefillTmCfg<D, NQ>;
   constexpr int BN = C::kBN;
   constexpr int RK = C::kRingK, RV = C::kRingV;
-  constexpr int kProducer = C::kSoftmaxWarps, kMma = C::kSoftmaxWarps + 1;
+  constexpr int kProducerK = C::kSoftmaxWarps, kProducerV = C::kSoftmaxWarps + 1;
+  constexpr int kMma = C::kSoftmaxWarps + 2;
   const AttnParams& p = pp.p;
   grid_dependency_wait();
   grid_launch_dependents();
@@ -181,61 +183,64 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   volatile int* abort_flag = &s_abort;
 
-  if (warp == kProducer) {
-    // ======================================================== TMA producer
+  if (warp == kProducerK || warp == kProducerV) {
+    // ======================================================== TMA producers (K, then V)
+    // Each warp streams one operand through its own ring, so a K tile never waits behind
+    // a V slot.  Block ids are loaded two tiles ahead and only checked when used, so the
+    // loop never stalls on a block-table load.
+    const bool is_k = warp == kProducerK;
+    const int R = is_k ? RK : RV;
+    uint64_t* const full = is_k ? k_full : v_full;
+    uint64_t* const empty = is_k ? k_empty : v_empty;
+    uint8_t* const ring = is_k ? sK : sV;
+    const CUtensorMap* const map = is_k ? &pp.tmap_k : &pp.tmap_v;
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
     const int bs = p.block_size;
     const int oob = p.num_blocks * bs;
-    if (lane == 0) {
+    if (is_k && lane == 0) {
       mbar_arrive_expect_tx(q_full, nq_act * C::kCB * TQ * G * 128);
       for (int qt = 0; qt < nq_act; ++qt)
         for (int cb = 0; cb < C::kCB; ++cb)
           tma_load_3d_pf(sQ + qt * C::kQBytes + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G,
                          q0 + t_first + qt * TQ, q_full);
     }
-    // cache row of this lane's 16-key page of key tile j (lanes 0 .. BN/16-1)
-    auto page_row = [&](int j) -> int {
+    // block id of this lane's 16-key page of key tile j (lanes 0 .. BN/16-1; -1: none)
+    auto page_blk = [&](int j) -> int {
+      const int key = ks + j * BN + 16 * lane;
+      const int col = key / bs;
+      return (j < nt && lane < BN / 16 && key < ke && col < p.max_blocks_per_seq) ? __ldg(bt + col) : -1;
+    };
+    // its cache row (the out-of-range row, zero-filled by the copy, where there is no key)
+    auto page_row = [&](int j, int blk) -> int {
       const int key = ks + j * BN + 16 * lane;
       if (lane >= BN / 16 || key >= ke) return oob;
-      const int col = key / bs;
-      const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
       if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
         atomicOr(p.status, DEV_BAD_BLOCK);
         return oob;
       }
       return blk * bs + key % bs;
     };
-    int row_next = nt > 0 ? page_row(0) : oob;
-    int k_issued = 0, v_issued = 0;
+    int blk0 = page_blk(0), blk1 = page_blk(1);
+    int issued = 0;
     for (int j = 0; j < nt; ++j) {
-      const int row = row_next;
-      if (j + 1 < nt) row_next = page_row(j + 1);
-      const int sk = j % RK, sv = j % RV;
-      if (j >= RK && !pf_wait_warp(&k_empty[sk], ((j / RK) - 1) & 1, abort_flag, p.status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
+      const int row = page_row(j, blk0);
+      blk0 = blk1;
+      blk1 = page_blk(j + 2);
+      const int sl = j % R;
+      if (j >= R && !pf_wait_warp(&empty[sl], ((j / R) - 1) & 1, abort_flag, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&full[sl], C::kTileBytes);
       __syncwarp();
       if (lane < BN / 16)
 #pragma unroll
         for (int cb = 0; cb < C::kCB; ++cb)
-          tma_load_3d_pf(sK + sk * C::kTileBytes + cb * C::kKVCB + lane * 2048, &pp.tmap_k,
-                         64 * cb, g, row, &k_full[sk]);
-      k_issued = j + 1;
-      if (j >= RV && !pf_wait_warp(&v_empty[sv], ((j / RV) - 1) & 1, abort_flag, p.status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
-      __syncwarp();
-      if (lane < BN / 16)
-#pragma unroll
-        for (int cb = 0; cb < C::kCB; ++cb)
-          tma_load_3d_pf(sV + sv * C::kTileBytes + cb * C::kKVCB + lane * 2048, &pp.tmap_v,
-                         64 * cb, g, row, &v_full[sv]);
-      v_issued = j + 1;
+          tma_load_3d_pf(ring + sl * C::kTileBytes + cb * C::kKVCB + lane * 2048, map, 64 * cb, g,
+                         row, &full[sl]);
+      issued = j + 1;
     }
     // never leave copies in flight into this CTA's shared memory (even after an abort)
-    for (int j = max(0, k_issued - RK); j < k_issued; ++j)
-      mbar_wait_bounded(&k_full[j % RK], (j / RK) & 1, p.status, DEV_TIMEOUT);
-    for (int j = max(0, v_issued - RV); j < v_issued; ++j)
-      mbar_wait_bounded(&v_full[j % RV], (j / RV) & 1, p.status, DEV_TIMEOUT);
-    if (lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
+    for (int j = max(0, issued - R); j < issued; ++j)
+      mbar_wait_bounded(&full[j % R], (j / R) & 1, p.status, DEV_TIMEOUT);
+    if (is_k && lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
   } else if (warp == kMma) {
     // ======================================================== MMA issuer
     // Step j: for each q tile, O += P V_{j-1} (which frees the tile's S/P columns), then
