@@ -49,23 +49,42 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def kernel_source_hash():
+# The source files each kernel is built from (a recorded ncu traffic figure stays valid
+# only while these are unchanged).
+KERNEL_SOURCES = {
+    "ua_attn_tile_kernel": ["ua_tile.cuh", "ua_tile_d*.cu", "ua_device.cuh", "ua_internal.h"],
+    "ua_prefill_tm_kernel": ["ua_prefill_tm.cuh", "ua_prefill.cuh", "ua_prefill_d64.cu",
+                             "ua_prefill_d128.cu", "ua_device.cuh", "ua_internal.h"],
+    "ua_prefill_tc_kernel": ["ua_prefill.cuh", "ua_prefill_d256.cu", "ua_device.cuh",
+                             "ua_internal.h"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "varlen_gqa_attention_paged_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+    files = sorted({f for pat in KERNEL_SOURCES[kernel] for f in glob.glob(os.path.join(csrc, pat))})
+    for p in files:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key):
+def kernel_name(plan, head_dim):
+    """The attention kernel a plan launches."""
+    if plan["kernel"] in (8, 16):
+        return "ua_prefill_tm_kernel" if head_dim <= 128 else "ua_prefill_tc_kernel"
+    return "ua_attn_tile_kernel"
+
+
+def recorded_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        rec = d[kernel_key]
-        if rec.get("source_hash") != kernel_source_hash():
+        rec = d[f"{kernel}/{workload}"]
+        if rec.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(rec["dram_bytes_per_launch"])
     except Exception:
@@ -256,7 +275,8 @@ def workload_record(inp, call, reps, attn_ms, total_ms, hbm_peak, tc_peak):
     med = statistics.median(total_ms)
     kbytes = W.kv_bytes_read(inp)
     flops = W.attention_flops(inp)
-    rec = {"path": "split" if call.plan["path"] == 2 else "2d", "n_part": call.plan["n_part"],
+    rec = {"kernel": kernel_name(call.plan, spec.head_dim),
+           "path": "split" if call.plan["path"] == 2 else "2d", "n_part": call.plan["n_part"],
            "kernel_block_m": call.plan["block_m"], "us_per_call": round(med * 1e3, 2),
            "attn_kernel_us": round(statistics.median(attn_ms) * 1e3, 2),
            "tokens_per_s": round(inp.total_q / (med * 1e-3), 1),
@@ -374,8 +394,17 @@ def run_ours(args):
     value = job_throughput(tokens_per_step, args.steps, elapsed_ms, world)
     attn_us = statistics.mean(attn_ms) * 1e3
     kbytes = W.kv_bytes_read(inp)
-    achieved = kbytes / (attn_us * 1e-6) / 1e9
-    kernel_key = f"ua_attn_tile_kernel/{spec.name}"
+    flops = W.attention_flops(inp)
+    kname = kernel_name(call.plan, spec.head_dim)
+    if kname == "ua_attn_tile_kernel":  # bandwidth-bound: algorithmic K/V bytes
+        achieved = kbytes / (attn_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "algorithmic_bytes_per_launch": kbytes}
+    else:  # dense contraction: algorithmic flops, dense bf16 peak (burst: the kernel is timed alone)
+        achieved = flops / (attn_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_burst,
+                "unit": "TFLOP/s", "frac": round(achieved / tc_burst, 4),
+                "algorithmic_flops_per_launch": flops}
     cpu = cpu_baseline(inp, budget_s=args.cpu_seconds)
     line = {
         "metric": "decode tokens/s (kernel-level, whole job)",
@@ -388,7 +417,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}.get(spec.kv_dtype, "f16 (e4m3 KV)"),
         "data": "synthetic (seeded N(0,1) q/k/v, shuffled block table)",
         "config": {"workload": spec.name, "desc": spec.desc, "batch": len(spec.seqs),
                    "q_len": spec.seqs[0][0], "kv_len": spec.seqs[0][1], "window": spec.window,
@@ -400,11 +429,9 @@ def run_ours(args):
                          f"step i reads replica i mod {reps}",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs": round(kbytes * args.steps / (elapsed_ms * 1e-3) / 1e9, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": recorded_traffic(kernel_key), "peak_source": peak_kind,
-                     "kernel": "ua_attn_tile_kernel (split-KV partition)",
-                     "algorithmic_bytes_per_launch": kbytes,
+        "roofline": {**roof,
+                     "traffic": recorded_traffic(kname, spec.name), "peak_source": peak_kind,
+                     "kernel": kname + (" (split-KV partition)" if call.plan["path"] == 2 else ""),
                      "kernel_us_mean": round(attn_us, 3),
                      "kernel_timing": "CUDA events around the attention kernel, every step of "
                                       "a pass of the same K steps right after the timed region",
