@@ -94,7 +94,7 @@ def test_dispatcher_splits_long_underfilled_decode():
 
 
 def test_dispatcher_keeps_short_or_full_grids_on_2d():
-    # short walk (below two minimum partitions of 128 keys): no split
+    # short walk (below two minimum partitions of 256 keys): no split
     assert _plan(max_seqlen_k=200, window_left=-1)["path"] == _lib.UA_PATH_2D
     # long prefill: the 2D grid already fills the device
     p = _plan(num_seqs=5, total_q=18432, max_seqlen_q=4096, max_seqlen_k=18432, window_left=-1)

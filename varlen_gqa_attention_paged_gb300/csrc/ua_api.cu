@@ -21,7 +21,7 @@ __device__ unsigned int g_device_status = 0;
 
 // Keys per split partition below which splitting a q-block's walk does not pay: the
 // partition must amortise its prologue and the extra merge traffic.
-constexpr int kMinPartitionKeys = 128;
+constexpr int kMinPartitionKeys = 256;
 constexpr int kMaxPartitions = 128;
 
 int device_sm_count(int* out) {

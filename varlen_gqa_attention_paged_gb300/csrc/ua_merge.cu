@@ -26,10 +26,17 @@ __global__ void __launch_bounds__(256) ua_merge_kernel(const __grid_constant__ M
   const int np = p.n_part;
   const float* m = p.ws_m + static_cast<size_t>(row) * np;
   const float* l = p.ws_l + static_cast<size_t>(row) * np;
+  const float* a = p.ws_acc + static_cast<size_t>(row) * np * D + lane * kPer;
 
+  // Partitions go 32 at a time, one per lane: max and sum loads are independent, the
+  // row max and sum are warp reductions, and every partition's weight reaches the lanes
+  // through a shuffle, so the partial-output loads of all partitions can be in flight
+  // together.  Empty partitions (l = 0) get weight 0 and are selected away.
   float M = -INFINITY;
-  for (int z = lane; z < np; z += 32)
-    if (l[z] > 0.f) M = fmaxf(M, m[z]);
+  for (int z0 = 0; z0 < np; z0 += 32) {
+    const int z = z0 + lane;
+    if (z < np && l[z] > 0.f) M = fmaxf(M, m[z]);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
@@ -38,20 +45,26 @@ __global__ void __launch_bounds__(256) ua_merge_kernel(const __grid_constant__ M
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
-    const float* a = p.ws_acc + static_cast<size_t>(row) * np * D + lane * kPer;
-    for (int z = 0; z < np; ++z) {
-      const float lz = l[z];
-      if (!(lz > 0.f)) continue;
-      const float wt = fast_exp2(m[z] - M);
-      L += lz * wt;
-      const float* az = a + static_cast<size_t>(z) * D;
+    for (int z0 = 0; z0 < np; z0 += 32) {
+      const int z = z0 + lane;
+      const float lz = z < np ? l[z] : 0.f;
+      const float wz = lz > 0.f ? fast_exp2(m[z] - M) : 0.f;
+      L += lz * wz;
+      const int nz = min(32, np - z0);
+#pragma unroll 8
+      for (int k = 0; k < nz; ++k) {
+        const float wt = __shfl_sync(0xffffffffu, wz, k);
+        const float* az = a + static_cast<size_t>(z0 + k) * D;
 #pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        const float2 v = *reinterpret_cast<const float2*>(az + e);
-        acc[e] += v.x * wt;
-        acc[e + 1] += v.y * wt;
+        for (int e = 0; e < kPer; e += 2) {
+          const float2 v = *reinterpret_cast<const float2*>(az + e);
+          acc[e] += wt != 0.f ? v.x * wt : 0.f;
+          acc[e + 1] += wt != 0.f ? v.y * wt : 0.f;
+        }
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const size_t base = static_cast<size_t>(row) * D + lane * kPer;
