@@ -77,7 +77,7 @@ struct TileCfg {
   static constexpr int kConvCB = 16 * 128;                 // f16 column block of 16 rows
   static constexpr int kConvWarpBytes = 2 * (D / 64) * kConvCB;  // K16 + V16 of one chunk
   static constexpr int kConvBytes = (KV == KV_E4M3) ? kConsumerWarps * kConvWarpBytes : 0;
-  static constexpr int kMergeBytes = (kWN > 1) ? kConsumerWarps * 16 * (D + 2) * 4 : 0;
+  static constexpr int kMergeBytes = (kWN > 1) ? kConsumerWarps * (2 * 16 + (D / 8) * 32 * 4) * 4 : 0;
   // decode-shaped CTAs aim at two per SM (about 110 KB each); the 64-row variant at one
   static constexpr int kBudget = (WM == 1 ? 110 : 200) * 1024;
   static constexpr int kStagesFit = (kBudget - kConvBytes) / kStageBytes;
@@ -627,72 +627,88 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
       }
     }
   } else {
-    // Four warps hold the same 16 rows over different keys: merge through shared memory
-    // (the pipeline buffers are free: every copy landed and every consumer is done).
-    float* sm_m = reinterpret_cast<float*>(pipe);
-    float* sm_l = sm_m + C::kConsumerWarps * 16;
-    float* sm_o = sm_l + C::kConsumerWarps * 16;
+    // Four warps hold the same 16 rows over different keys (the pipeline buffers are free:
+    // every copy landed and every consumer is done).  Each warp rescales its state to the
+    // rows' max (exchanged through shared memory); warp 0 adds the others' partial sums,
+    // read in the MMA fragment layout (conflict-free), and writes the rows.
+    float* sm_m = reinterpret_cast<float*>(pipe);                      // [4][16]
+    float* sm_l = sm_m + C::kConsumerWarps * 16;                       // [4][16]
+    float4* sm_o = reinterpret_cast<float4*>(sm_l + C::kConsumerWarps * 16);  // [4][D/8][32]
+    if (cq == 0) {
+      sm_m[warp * 16 + gq] = m_run[0];
+      sm_m[warp * 16 + gq + 8] = m_run[1];
+    }
+    named_bar_sync(1, 32 * C::kConsumerWarps);
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int row = gq + 8 * rr;
-      if (cq == 0) {
-        sm_m[warp * 16 + row] = m_run[rr];
-        sm_l[warp * 16 + row] = l_run[rr];
-      }
-#pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        const int col = nd * 8 + 2 * cq;
-        *reinterpret_cast<float2*>(sm_o + (warp * 16 + row) * D + col) =
-            make_float2(o_acc[nd][2 * rr], o_acc[nd][2 * rr + 1]);
-      }
-    }
-    named_bar_sync(1, 32 * C::kConsumerWarps);
-    const int tid = threadIdx.x;  // 0..127
-    for (int idx = tid; idx < 16 * (D / 4); idx += 32 * C::kConsumerWarps) {
-      const int row = idx / (D / 4);
-      const int col = (idx % (D / 4)) * 4;
-      const int r = r0 + row;
-      if (r >= r1 || q0 + r / G >= p.total_q) continue;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * 16 + row]);
-      float L = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (M != -INFINITY) {
+      const float wt = M == -INFINITY ? 0.f : fast_exp2(m_run[rr] - M);
+      m_run[rr] = M;
+      l_run[rr] *= wt;
 #pragma unroll
-        for (int w = 0; w < C::kConsumerWarps; ++w) {
-          const float wt = fast_exp2(sm_m[w * 16 + row] - M);
-          L += sm_l[w * 16 + row] * wt;
-          const float4 o4 = *reinterpret_cast<const float4*>(sm_o + (w * 16 + row) * D + col);
-          acc.x += o4.x * wt;
-          acc.y += o4.y * wt;
-          acc.z += o4.z * wt;
-          acc.w += o4.w * wt;
-        }
+      for (int nd = 0; nd < D / 8; ++nd) {
+        o_acc[nd][2 * rr] *= wt;
+        o_acc[nd][2 * rr + 1] *= wt;
       }
-      const int i = r / G;
-      const size_t orow = static_cast<size_t>(q0 + i) * p.hq + g * G + r % G;
+    }
+    if (warp != 0) {
+      if (cq == 0) {
+        sm_l[warp * 16 + gq] = l_run[0];
+        sm_l[warp * 16 + gq + 8] = l_run[1];
+      }
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd)
+        sm_o[(warp * (D / 8) + nd) * 32 + lane] =
+            make_float4(o_acc[nd][0], o_acc[nd][1], o_acc[nd][2], o_acc[nd][3]);
+    }
+    named_bar_sync(1, 32 * C::kConsumerWarps);
+    if (warp != 0) return;
+#pragma unroll
+    for (int w = 1; w < C::kConsumerWarps; ++w) {
+      l_run[0] += sm_l[w * 16 + gq];
+      l_run[1] += sm_l[w * 16 + gq + 8];
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const float4 o4 = sm_o[(w * (D / 8) + nd) * 32 + lane];
+        o_acc[nd][0] += o4.x;
+        o_acc[nd][1] += o4.y;
+        o_acc[nd][2] += o4.z;
+        o_acc[nd][3] += o4.w;
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      if (!rv[rr]) continue;
+      const size_t row = static_cast<size_t>(rt[rr]) * p.hq + rh[rr];
       if (n_part == 1) {
-        const float inv = L > 0.f ? v_scale / L : 0.f;
-        const float x0 = acc.x * inv, x1 = acc.y * inv, x2 = acc.z * inv, x3 = acc.w * inv;
-        if (p.out_dtype == UA_DT_F32) {
-          *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + col) =
-              make_float4(x0, x1, x2, x3);
-        } else if (p.out_dtype == UA_DT_BF16) {
-          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * D + col) =
-              make_uint2(pack_bf16(x0, x1), pack_bf16(x2, x3));
-        } else {
-          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * D + col) =
-              make_uint2(pack_f16(x0, x1), pack_f16(x2, x3));
+        const float inv = l_run[rr] > 0.f ? v_scale / l_run[rr] : 0.f;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) {
+          const int col = nd * 8 + 2 * cq;
+          const float x0 = o_acc[nd][2 * rr] * inv, x1 = o_acc[nd][2 * rr + 1] * inv;
+          if (p.out_dtype == UA_DT_F32) {
+            *reinterpret_cast<float2*>(static_cast<float*>(p.out) + row * D + col) =
+                make_float2(x0, x1);
+          } else {
+            const uint32_t v = p.out_dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
+            *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + col) = v;
+          }
         }
       } else {
-        const size_t w = orow * n_part + z;
-        if (col == 0) {
-          p.ws_m[w] = M;
-          p.ws_l[w] = L;
+        const size_t w = row * n_part + z;
+        if (cq == 0) {
+          p.ws_m[w] = m_run[rr];
+          p.ws_l[w] = l_run[rr];
         }
-        *reinterpret_cast<float4*>(p.ws_acc + w * D + col) =
-            make_float4(acc.x * v_scale, acc.y * v_scale, acc.z * v_scale, acc.w * v_scale);
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) {
+          const int col = nd * 8 + 2 * cq;
+          *reinterpret_cast<float2*>(p.ws_acc + w * D + col) =
+              make_float2(o_acc[nd][2 * rr] * v_scale, o_acc[nd][2 * rr + 1] * v_scale);
+        }
       }
     }
   }
