@@ -55,8 +55,8 @@ KERNEL_SOURCES = {
     "ua_attn_tile_kernel": ["ua_tile.cuh", "ua_tile_d*.cu", "ua_device.cuh", "ua_internal.h"],
     "ua_prefill_tm_kernel": ["ua_prefill_tm.cuh", "ua_prefill.cuh", "ua_prefill_d64.cu",
                              "ua_prefill_d128.cu", "ua_device.cuh", "ua_internal.h"],
-    "ua_prefill_tc_kernel": ["ua_prefill.cuh", "ua_prefill_d256.cu", "ua_device.cuh",
-                             "ua_internal.h"],
+    "ua_prefill_wide_kernel": ["ua_prefill_wide.cuh", "ua_prefill.cuh", "ua_prefill_d256.cu",
+                               "ua_device.cuh", "ua_internal.h"],
 }
 
 
@@ -73,7 +73,7 @@ def kernel_source_hash(kernel):
 def kernel_name(plan, head_dim):
     """The attention kernel a plan launches."""
     if plan["kernel"] in (8, 16):
-        return "ua_prefill_tm_kernel" if head_dim <= 128 else "ua_prefill_tc_kernel"
+        return "ua_prefill_tm_kernel" if head_dim <= 128 else "ua_prefill_wide_kernel"
     return "ua_attn_tile_kernel"
 
 

@@ -116,6 +116,12 @@ SMALL = {
                                   qq_bias=True, qq_bias_shape=(64, 64), sinks=True),
     "pf_f16_g6_chunk": dict(seqs=[(70, 600), (1, 17)], num_q_heads=12, num_kv_heads=2,
                             window=300),
+    # head_dim 256: K and V stream as half tiles through one ring; odd and even tile counts
+    "pf_f16_d256_ragged": dict(seqs=[(130, 390), (1, 129), (64, 64), (257, 900)],
+                               num_q_heads=8, num_kv_heads=2, head_dim=256),
+    "pf_bf16_d256_mha_window_sinks": dict(seqs=[(300, 700), (17, 17)], num_q_heads=4,
+                                          num_kv_heads=4, head_dim=256, q_dtype=torch.bfloat16,
+                                          kv_dtype=torch.bfloat16, window=200, sinks=True),
 }
 
 

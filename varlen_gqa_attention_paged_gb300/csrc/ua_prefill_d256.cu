@@ -1,11 +1,12 @@
 // ua_prefill_d256.cu -- instantiations of the tensor-memory prefill kernel for head_dim 256.
-#include "ua_prefill.cuh"
+#include "ua_prefill_wide.cuh"
 
 namespace ua {
 
 cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
                                 cudaStream_t s) {
-  return launch_prefill_dispatch<256>(pp, grid, kv, feat, nq, s);
+  if (nq != 1) return cudaErrorInvalidValue;
+  return launch_prefill_wide_dispatch<256>(pp, grid, kv, feat, s);
 }
 
 }  // namespace ua
