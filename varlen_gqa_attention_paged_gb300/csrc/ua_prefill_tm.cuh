@@ -402,9 +402,9 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
           tmem_st32(tS + c0 + 32, rb);
         }
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          mx0 = fmaxf(mx0, __uint_as_float(ra[e]));
-          mx1 = fmaxf(mx1, __uint_as_float(rb[e]));
+        for (int e = 0; e < 32; e += 2) {
+          mx0 = fmax3(mx0, __uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(rb[e]), __uint_as_float(rb[e + 1]));
         }
       }
       if (rewrite) tmem_st_wait();

@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
   uint64_t* const p_full = bars + 5;                  // [2]: P in S buffer b ready
   uint64_t* const full = bars + 7;                    // [NS]
   uint64_t* const empty = full + NS;                  // [NS]
-  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(empty + NS);
+  uint64_t* const lo_bar = empty + NS;                // the softmax warps agree on P's low part
+  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(lo_bar + 1);
   int* const lo_flag = reinterpret_cast<int*>(tmem_holder + 1);  // [2]: step + 1 when P_lo matters
   __shared__ int s_abort;
   __shared__ int s_last[C::kProducers];  // last item each producer warp issued
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
     mbar_init(pv_done, 1);
+    mbar_init(lo_bar, 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
@@ -391,9 +393,9 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
           tmem_st32(tS + c0 + 32, rb);
         }
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          mx0 = fmaxf(mx0, __uint_as_float(ra[e]));
-          mx1 = fmaxf(mx1, __uint_as_float(rb[e]));
+        for (int e = 0; e < 32; e += 2) {
+          mx0 = fmax3(mx0, __uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(rb[e]), __uint_as_float(rb[e + 1]));
         }
       }
       if (rewrite) tmem_st_wait();
@@ -421,10 +423,21 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
         }
       }
       const float pmax = mx == -INFINITY ? 0.f : fast_exp2(mx - m_use);
-      const bool warp_lo = BF16 && __any_sync(0xffffffffu, pmax * 63.f > l * alpha);
+      // The tile's P carries a low part when any of its rows needs one: every warp of the
+      // tile then writes both parts, otherwise only the high part (the MMA reads the
+      // same flag).  The tile's four warps agree on it through an mbarrier.
+      bool tile_lo = false;
+      if constexpr (BF16) {
+        if (__any_sync(0xffffffffu, pmax * 63.f > l * alpha) && lane == 0)
+          lo_flag[bb] = j + 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(lo_bar);
+        if (!pf_wait_warp(lo_bar, j & 1, abort_flag, p.status)) { ok = false; break; }
+        tile_lo = lo_flag[bb] == j + 1;
+      }
 
       // ---- pass 2: P = 2^(c s - m) over S, 32 keys at a time (16 columns of high part,
-      // 16 of bf16 remainder or zeros)
+      // then, when the tile needs it, 16 of bf16 remainder)
       const float2 cc = make_float2(c, c), mm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll 1
@@ -446,23 +459,26 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
           acc0 = __fadd2_rn(acc0, make_float2(xv[e], xv[e + 1]));
           acc1 = __fadd2_rn(acc1, make_float2(xv[e + 2], xv[e + 3]));
         }
+        if (tile_lo) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t hw = BF16 ? pack_bf16(xv[2 * e], xv[2 * e + 1]) : pack_f16(xv[2 * e], xv[2 * e + 1]);
-          rr[e] = hw;
-          if (BF16 && warp_lo) {
+          for (int e = 0; e < 16; ++e) {
+            const uint32_t hw = pack_bf16(xv[2 * e], xv[2 * e + 1]);
+            rr[e] = hw;
             const float2 rem = __fadd2_rn(make_float2(xv[2 * e], xv[2 * e + 1]),
                                           make_float2(-bf16_lo(hw), -bf16_hi(hw)));
             rr[16 + e] = pack_bf16(rem.x, rem.y);
-          } else {
-            rr[16 + e] = 0u;
           }
+          tmem_st32(tS + c0, rr);
+        } else {
+          uint32_t hw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            hw[e] = BF16 ? pack_bf16(xv[2 * e], xv[2 * e + 1]) : pack_f16(xv[2 * e], xv[2 * e + 1]);
+          tmem_st16(tS + c0, hw);
         }
-        tmem_st32(tS + c0, rr);
       }
       l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
       tmem_st_wait();
-      if (warp_lo && lane == 0) lo_flag[bb] = j + 1;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[bb]);
