@@ -18,7 +18,9 @@
 //               reads below free of bank conflicts.
 //   warps 0..3  consumers: QK^T and P.V on tensor cores (mma.sync m16n8k16, fp32
 //               accumulate), score transform, online softmax in base 2 with quad
-//               shuffles, fp8 e4m3 -> f16 dequant of the tile in shared memory.
+//               shuffles.  fp8 e4m3 codes are turned into f16 MMA operands in
+//               registers: the head dimension is permuted so that every lane's operand
+//               bytes are contiguous in shared memory (see kPermD).
 //   WM = 1 (decode-shaped q-blocks, BM = 16): the four consumer warps share the 16
 //          rows and each takes 16 keys of every tile; their states merge at the end.
 //   WM = 4 (BM = 64): each consumer warp owns 16 rows and walks every key.
@@ -74,19 +76,22 @@ struct TileCfg {
   static constexpr int kCB = kRowBytes / kCBW;         // column blocks per row
   static constexpr int kCBBytes = kT * kCBW;           // one column block of a tile
   static constexpr int kStageBytes = 2 * kCB * kCBBytes;  // K then V
-  static constexpr int kConvCB = 16 * 128;                 // f16 column block of 16 rows
-  static constexpr int kConvWarpBytes = 2 * (D / 64) * kConvCB;  // K16 + V16 of one chunk
-  static constexpr int kConvBytes = (KV == KV_E4M3) ? kConsumerWarps * kConvWarpBytes : 0;
+  // fp8 operands are dequantised in registers, with the head dimension permuted: the
+  // QK^T sum runs over d in any order (Q and K permuted alike), and the P.V output
+  // columns are put back in order when written.
+  static constexpr bool kPermD = KV == KV_E4M3;
   static constexpr int kMergeBytes = (kWN > 1) ? kConsumerWarps * (2 * 16 + (D / 8) * 32 * 4) * 4 : 0;
   // decode-shaped CTAs aim at two per SM (about 110 KB each); the 64-row variant at one
   static constexpr int kBudget = (WM == 1 ? 110 : 200) * 1024;
-  static constexpr int kStagesFit = (kBudget - kConvBytes) / kStageBytes;
+  static constexpr int kStagesFit = kBudget / kStageBytes;
   static constexpr int kStages = kStagesFit < 2 ? 2 : (kStagesFit > 4 ? 4 : kStagesFit);
   static constexpr int kPipeRaw =
       (kStages * kStageBytes > kMergeBytes) ? kStages * kStageBytes : kMergeBytes;
   static constexpr int kPipeBytes = (kPipeRaw + 1023) & ~1023;
-  static constexpr int kSmemBytes = 1024 + kPipeBytes + kConvBytes + 2 * kStages * 8;
-  static constexpr int kMinBlocks = (2 * kSmemBytes <= 227 * 1024) ? 2 : 1;
+  static constexpr int kSmemBytes = 1024 + kPipeBytes + 2 * kStages * 8;
+  // two CTAs per SM when they fit, but not at d256, whose 16 x 256 fp32 accumulators alone
+  // take 128 registers a thread
+  static constexpr int kMinBlocks = (D <= 128 && 2 * kSmemBytes <= 227 * 1024) ? 2 : 1;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kRowBytes % kCBW == 0 && kCBW % 16 == 0, "rows are whole column blocks");
   static_assert(kSwz || KV == KV_E4M3, "16-bit rows are at least 128 bytes");
@@ -96,7 +101,51 @@ struct TileCfg {
     if constexpr (kSwz) return (c / 8) * kCBBytes + sw128(r, c % 8);
     else return r * kCBW + c * 16;
   }
+  // Byte offset of byte `x` of tile row r (x % 16 + the 16-byte chunk's offset).
+  static __device__ __forceinline__ uint32_t raw_byte(uint32_t r, uint32_t x) {
+    return raw_off(r, x / 16) + (x & 15u);
+  }
 };
+
+// Writes row rr (0: fragment row gq, 1: gq + 8) of a warp's P.V accumulators times `mul`
+// to `dst` (D values of type `dtype`).  Fragment column 2cq + e of n-tile nd is output
+// column 8 nd + 2cq + e, or (2cq + e) D/8 + nd when the head dimension is permuted.
+template <int D, bool PERM>
+__device__ __forceinline__ void store_o_row(const float (&o)[D / 8][4], int rr, int cq, float mul,
+                                            void* dst, int dtype) {
+  if constexpr (!PERM) {
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      const int col = nd * 8 + 2 * cq;
+      const float x0 = o[nd][2 * rr] * mul, x1 = o[nd][2 * rr + 1] * mul;
+      if (dtype == UA_DT_F32) {
+        *reinterpret_cast<float2*>(static_cast<float*>(dst) + col) = make_float2(x0, x1);
+      } else {
+        const uint32_t v = dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
+        *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(dst) + col) = v;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int base = (2 * cq + e) * (D / 8);
+#pragma unroll
+      for (int nd = 0; nd < D / 8; nd += 4) {
+        const float x0 = o[nd][2 * rr + e] * mul, x1 = o[nd + 1][2 * rr + e] * mul;
+        const float x2 = o[nd + 2][2 * rr + e] * mul, x3 = o[nd + 3][2 * rr + e] * mul;
+        if (dtype == UA_DT_F32) {
+          *reinterpret_cast<float4*>(static_cast<float*>(dst) + base + nd) =
+              make_float4(x0, x1, x2, x3);
+        } else {
+          const bool bf = dtype == UA_DT_BF16;
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(dst) + base + nd) =
+              make_uint2(bf ? pack_bf16(x0, x1) : pack_f16(x0, x1),
+                         bf ? pack_bf16(x2, x3) : pack_f16(x2, x3));
+        }
+      }
+    }
+  }
+}
 
 // Sequence owning q-block slot x: the last b with floor(cu[b] * G / BM) + b <= x
 // (a monotone slot layout that leaves at most one idle slot per sequence).
@@ -152,8 +201,7 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* const pipe = smem;
-  uint8_t* const conv = smem + C::kPipeBytes;
-  uint64_t* const full = reinterpret_cast<uint64_t*>(conv + C::kConvBytes);
+  uint64_t* const full = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
   uint64_t* const empty = full + S;
   __shared__ int s_abort;
 
@@ -351,7 +399,9 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int rr = j & 1;
-      const int col = kk * 16 + 2 * cq + 8 * (j >> 1);
+      // fp8: k-slice kk of lane cq is d = cq D/4 + 4 kk + {0..3} (the K bytes it reads)
+      const int col = C::kPermD ? cq * (D / 4) + 4 * kk + 2 * (j >> 1)
+                                : kk * 16 + 2 * cq + 8 * (j >> 1);
       uint32_t v = 0;
       if (rv[rr]) {
         const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
@@ -389,8 +439,6 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
 #pragma unroll
     for (int e = 0; e < 4; ++e) o_acc[nd][e] = 0.f;
 
-  uint8_t* const conv_k = conv + warp * C::kConvWarpBytes;
-  uint8_t* const conv_v = conv_k + (D / 64) * C::kConvCB;
   // Cache slots at or past kv_len in the sequence's last page hold no key and may hold
   // anything (NaN included): their P is 0, and their V values are zeroed before P.V so
   // that 0 * NaN never enters the accumulator.
@@ -411,61 +459,39 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
       const int kc0 = key_tile + 16 * ch;
       if (!tile_any || kc0 >= ke || kc0 > pmax || kc0 + 16 <= lomin) continue;
 
-      uint32_t kbase, vbase, cbk;
-      int row0;
-      if constexpr (KV == KV_E4M3) {
-        // Dequantise the chunk's 16 K rows and 16 V rows to f16 (exact); the scales
-        // are applied to the scores and to the output instead.  V rows past kv_len
-        // become zero here.  Each lane turns 16 codes into two 16-byte f16 chunks.
-        __syncwarp();
-#pragma unroll 2
-        for (int it = 0; it < (2 * 16 * D / 16) / 32; ++it) {
-          const int idx = it * 32 + lane;
-          const int which = idx / D;  // 0: K, 1: V  (16 rows x D/16 groups each)
-          const int rem = idx % D;
-          const int row = rem / (D / 16), grp = rem % (D / 16);
-          const int trow = 16 * ch + row;
-          uint4 raw = *reinterpret_cast<const uint4*>((which ? vst : kst) + C::raw_off(trow, grp));
-          if (which && kc0 + row >= kv_len) raw = make_uint4(0, 0, 0, 0);
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t h[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            h[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] & 0xffffu));
-            h[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16));
-          }
-          uint8_t* dst = (which ? conv_v : conv_k) + (grp / 4) * C::kConvCB;
-          const int c16 = (grp % 4) * 2;
-          *reinterpret_cast<uint4*>(dst + sw128(row, c16)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(dst + sw128(row, c16 + 1)) =
-              make_uint4(h[4], h[5], h[6], h[7]);
-        }
-        __syncwarp();
-        kbase = smem_addr(conv_k);
-        vbase = smem_addr(conv_v);
-        cbk = C::kConvCB;
-        row0 = 0;
-      } else {
-        kbase = smem_addr(kst);
-        vbase = smem_addr(vst);
-        cbk = C::kCBBytes;
-        row0 = 16 * ch;
-      }
-
       // ---- S = Q K^T for 16 keys (two n8 chunks)
       float sc[2][4];
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[n][e] = 0.f;
-      {
-        const uint32_t kr = row0 + (lane & 7) + ((lane >> 4) << 3);
+      if constexpr (C::kPermD) {
+        // Lane (gq, cq) reads bytes [cq D/4, (cq + 1) D/4) of K rows gq and gq + 8: word
+        // q of its 16-byte chunk u holds d = cq D/4 + 4 kk + {0..3} of k-slice kk = 4u + q,
+        // i.e. the B operand pairs (2cq, 2cq+1) and (2cq+8, 2cq+9) of that slice.
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const uint32_t trow = 16 * ch + gq + 8 * n;
+#pragma unroll
+          for (int u = 0; u < D / 64; ++u) {
+            const uint4 raw =
+                *reinterpret_cast<const uint4*>(kst + C::raw_byte(trow, cq * (D / 4) + 16 * u));
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              mma_16816<true>(sc[n], qf[4 * u + q], e4m3x2_to_f16x2(static_cast<uint16_t>(w[q])),
+                              e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16)));
+          }
+        }
+      } else {
+        const uint32_t kbase = smem_addr(kst);
+        const uint32_t kr = 16 * ch + (lane & 7) + ((lane >> 4) << 3);
         const uint32_t half = (lane >> 3) & 1;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t c = (kk & 3) * 2 + half;  // 16-byte chunk within the column block
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kbase + (kk >> 2) * cbk + sw128(kr, c), b0, b1, b2, b3);
+          ldsm_x4(kbase + (kk >> 2) * C::kCBBytes + sw128(kr, c), b0, b1, b2, b3);
           mma_16816<kF16Mma>(sc[0], qf[kk], b0, b1);
           mma_16816<kF16Mma>(sc[1], qf[kk], b2, b3);
         }
@@ -499,18 +525,22 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
         }
       }
 
-      // ---- online softmax (rows gq, gq + 8; a row's 16 scores sit in one quad)
+      // ---- online softmax (rows gq, gq + 8; a row's 16 scores sit in one quad).  A row's
+      // running max moves only when a score passes it by more than 8 (log2 units), so P
+      // stays below 2^8 and the accumulators are rescaled only on those chunks.
       float alpha[2];
+      bool grow_any = false;
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         float mx = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]),
                          fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run[rr], mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        alpha[rr] = fast_exp2(m_run[rr] - m_use);
-        m_run[rr] = m_new;
+        const bool grow = mx > m_run[rr] + 8.f;  // from -inf: the first finite score
+        alpha[rr] = grow ? fast_exp2(m_run[rr] - mx) : 1.f;
+        if (grow) m_run[rr] = mx;
+        grow_any |= grow;
+        const float m_use = (m_run[rr] == -INFINITY) ? 0.f : m_run[rr];
         float rs = 0.f;
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
@@ -520,12 +550,14 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
         }
         l_run[rr] = l_run[rr] * alpha[rr] + rs;
       }
+      if (__any_sync(0xffffffffu, grow_any)) {
 #pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        o_acc[nd][0] *= alpha[0];
-        o_acc[nd][1] *= alpha[0];
-        o_acc[nd][2] *= alpha[1];
-        o_acc[nd][3] *= alpha[1];
+        for (int nd = 0; nd < D / 8; ++nd) {
+          o_acc[nd][0] *= alpha[0];
+          o_acc[nd][1] *= alpha[0];
+          o_acc[nd][2] *= alpha[1];
+          o_acc[nd][3] *= alpha[1];
+        }
       }
 
       // ---- O += P V  (P as the A operand straight from the S accumulators)
@@ -546,32 +578,75 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
         }
       }
       {
-        const uint32_t vr = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const uint32_t dh = lane >> 4;
         const int k0 = kc0 + 2 * cq;
         const bool tail = kc0 + 16 > kv_len;
         // b0/b2 hold keys k0, k0+1 and b1/b3 keys k0+8, k0+9 of the chunk
         const uint32_t m01 = (k0 < kv_len ? 0xffffu : 0u) | (k0 + 1 < kv_len ? 0xffff0000u : 0u);
         const uint32_t m89 =
             (k0 + 8 < kv_len ? 0xffffu : 0u) | (k0 + 9 < kv_len ? 0xffff0000u : 0u);
+        if constexpr (C::kPermD) {
+          // Lane (gq, cq) reads bytes [gq D/8, (gq + 1) D/8) of V rows 2cq, 2cq+1, 2cq+8,
+          // 2cq+9: byte nd of them is output column gq D/8 + nd (fragment column gq of
+          // n-tile nd).  A byte permute pairs the two keys of each B operand half.
+          constexpr int kW = D / 32;  // 32-bit words of a row per lane
+          uint32_t vw[4][kW];
 #pragma unroll
-        for (int nd = 0; nd < D / 8; nd += 2) {
-          const uint32_t c = (nd & 7) + dh;  // 16-byte chunk within the column block
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(vbase + (nd >> 3) * cbk + sw128(vr, c), b0, b1, b2, b3);
-          if constexpr (KV != KV_E4M3) {
+          for (int r4 = 0; r4 < 4; ++r4) {
+            const uint32_t trow = 16 * ch + 2 * cq + (r4 & 1) + 8 * (r4 >> 1);
+            if constexpr (kW % 4 == 0) {
+#pragma unroll
+              for (int x = 0; x < kW; x += 4) {
+                const uint4 v4 =
+                    *reinterpret_cast<const uint4*>(vst + C::raw_byte(trow, gq * (D / 8) + 4 * x));
+                vw[r4][x] = v4.x;
+                vw[r4][x + 1] = v4.y;
+                vw[r4][x + 2] = v4.z;
+                vw[r4][x + 3] = v4.w;
+              }
+            } else {
+              const uint2 v2 = *reinterpret_cast<const uint2*>(vst + C::raw_byte(trow, gq * (D / 8)));
+              vw[r4][0] = v2.x;
+              vw[r4][1] = v2.y;
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < kW; ++x) {
+            const uint32_t p0[2] = {__byte_perm(vw[0][x], vw[1][x], 0x5140),
+                                    __byte_perm(vw[0][x], vw[1][x], 0x7362)};
+            const uint32_t p1[2] = {__byte_perm(vw[2][x], vw[3][x], 0x5140),
+                                    __byte_perm(vw[2][x], vw[3][x], 0x7362)};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(p0[q >> 1] >> (16 * (q & 1))));
+              uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(p1[q >> 1] >> (16 * (q & 1))));
+              if (tail) {
+                b0 &= m01;
+                b1 &= m89;
+              }
+              mma_16816<true>(o_acc[4 * x + q], pa, b0, b1);
+            }
+          }
+        } else {
+          const uint32_t vbase = smem_addr(vst);
+          const uint32_t vr = 16 * ch + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const uint32_t dh = lane >> 4;
+#pragma unroll
+          for (int nd = 0; nd < D / 8; nd += 2) {
+            const uint32_t c = (nd & 7) + dh;  // 16-byte chunk within the column block
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(vbase + (nd >> 3) * C::kCBBytes + sw128(vr, c), b0, b1, b2, b3);
             if (tail) {
               b0 &= m01;
               b2 &= m01;
               b1 &= m89;
               b3 &= m89;
             }
-          }
-          mma_16816<kF16Mma>(o_acc[nd], pa, b0, b1);
-          mma_16816<kF16Mma>(o_acc[nd + 1], pa, b2, b3);
-          if constexpr (!kF16Mma) {
-            mma_16816<kF16Mma>(o_acc[nd], pl, b0, b1);
-            mma_16816<kF16Mma>(o_acc[nd + 1], pl, b2, b3);
+            mma_16816<kF16Mma>(o_acc[nd], pa, b0, b1);
+            mma_16816<kF16Mma>(o_acc[nd + 1], pa, b2, b3);
+            if constexpr (!kF16Mma) {
+              mma_16816<kF16Mma>(o_acc[nd], pl, b0, b1);
+              mma_16816<kF16Mma>(o_acc[nd + 1], pl, b2, b3);
+            }
           }
         }
       }
@@ -600,30 +675,16 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
       const size_t row = static_cast<size_t>(rt[rr]) * p.hq + rh[rr];
       if (n_part == 1) {
         const float inv = l_run[rr] > 0.f ? v_scale / l_run[rr] : 0.f;
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          const int col = nd * 8 + 2 * cq;
-          const float x0 = o_acc[nd][2 * rr] * inv, x1 = o_acc[nd][2 * rr + 1] * inv;
-          if (p.out_dtype == UA_DT_F32) {
-            *reinterpret_cast<float2*>(static_cast<float*>(p.out) + row * D + col) =
-                make_float2(x0, x1);
-          } else {
-            const uint32_t v = p.out_dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
-            *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + col) = v;
-          }
-        }
+        const size_t esz = p.out_dtype == UA_DT_F32 ? 4 : 2;
+        store_o_row<D, C::kPermD>(o_acc, rr, cq, inv, static_cast<uint8_t*>(p.out) + row * D * esz,
+                                  p.out_dtype);
       } else {
         const size_t w = row * n_part + z;
         if (cq == 0) {
           p.ws_m[w] = m_run[rr];
           p.ws_l[w] = l_run[rr];
         }
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          const int col = nd * 8 + 2 * cq;
-          *reinterpret_cast<float2*>(p.ws_acc + w * D + col) =
-              make_float2(o_acc[nd][2 * rr] * v_scale, o_acc[nd][2 * rr + 1] * v_scale);
-        }
+        store_o_row<D, C::kPermD>(o_acc, rr, cq, v_scale, p.ws_acc + w * D, UA_DT_F32);
       }
     }
   } else {
@@ -685,30 +746,16 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
       const size_t row = static_cast<size_t>(rt[rr]) * p.hq + rh[rr];
       if (n_part == 1) {
         const float inv = l_run[rr] > 0.f ? v_scale / l_run[rr] : 0.f;
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          const int col = nd * 8 + 2 * cq;
-          const float x0 = o_acc[nd][2 * rr] * inv, x1 = o_acc[nd][2 * rr + 1] * inv;
-          if (p.out_dtype == UA_DT_F32) {
-            *reinterpret_cast<float2*>(static_cast<float*>(p.out) + row * D + col) =
-                make_float2(x0, x1);
-          } else {
-            const uint32_t v = p.out_dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
-            *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + col) = v;
-          }
-        }
+        const size_t esz = p.out_dtype == UA_DT_F32 ? 4 : 2;
+        store_o_row<D, C::kPermD>(o_acc, rr, cq, inv, static_cast<uint8_t*>(p.out) + row * D * esz,
+                                  p.out_dtype);
       } else {
         const size_t w = row * n_part + z;
         if (cq == 0) {
           p.ws_m[w] = m_run[rr];
           p.ws_l[w] = l_run[rr];
         }
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          const int col = nd * 8 + 2 * cq;
-          *reinterpret_cast<float2*>(p.ws_acc + w * D + col) =
-              make_float2(o_acc[nd][2 * rr] * v_scale, o_acc[nd][2 * rr + 1] * v_scale);
-        }
+        store_o_row<D, C::kPermD>(o_acc, rr, cq, v_scale, p.ws_acc + w * D, UA_DT_F32);
       }
     }
   }
