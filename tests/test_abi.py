@@ -119,7 +119,7 @@ def test_dispatcher_split_fits_one_wave():
     for hkv, seqs, kv in ((8, 8, 1), (2, 4, 0), (8, 2, 2), (1, 1, 1)):
         p = _plan(num_seqs=seqs, total_q=seqs, num_kv_heads=hkv, num_q_heads=4 * hkv, kv_dtype=kv,
                   window_left=-1, max_seqlen_k=100000)
-        active = seqs * hkv
+        active = seqs * p["grid_y"]                     # CTAs of one partition
         assert p["path"] == _lib.UA_PATH_SPLIT
         assert active * p["n_part"] <= 2 * 152            # two CTAs per SM at most
         # the largest count that fits: one more partition would start a second wave

@@ -122,6 +122,17 @@ SMALL = {
     "pf_bf16_d256_mha_window_sinks": dict(seqs=[(300, 700), (17, 17)], num_q_heads=4,
                                           num_kv_heads=4, head_dim=256, q_dtype=torch.bfloat16,
                                           kv_dtype=torch.bfloat16, window=200, sinks=True),
+    # decode-shaped q-blocks (at most 8 rows per kv-head) with every score feature, a row
+    # with no key, partial pages; 128-byte cache rows (fp8 at d128, 16-bit at d64)
+    "dec_fp8_feat": dict(seqs=[(1, 700), (2, 129), (1, 1), (1, 17), (1, 0), (4, 333)],
+                          num_q_heads=8, num_kv_heads=4, kv_dtype=torch.float8_e4m3fn,
+                          q_dtype=torch.bfloat16, softcap=25.0, alibi=True, qq_bias=True,
+                          qq_bias_shape=(8, 16), sinks=True, window=260),
+    "dec_bf16_d64_window": dict(seqs=[(1, 900), (4, 300), (1, 65)], num_q_heads=8,
+                                 num_kv_heads=4, head_dim=64, q_dtype=torch.bfloat16,
+                                 kv_dtype=torch.bfloat16, window=200, sinks=True),
+    "dec_f16_d64_g8": dict(seqs=[(1, 500), (1, 31), (1, 16)], num_q_heads=16, num_kv_heads=2,
+                            head_dim=64, block_size=32),
 }
 
 
@@ -144,9 +155,11 @@ def test_forced_partition_counts(n_part):
     assert max_err(out, want) <= 2e-3
 
 
-@pytest.mark.parametrize("kv", [torch.float16, torch.float8_e4m3fn])
-def test_block_table_permutation_is_bit_exact(kv):
-    spec = _small(7, kv_dtype=kv, window=100, sinks=True, num_blocks=80)
+@pytest.mark.parametrize("kv,decode", [(torch.float16, False), (torch.float8_e4m3fn, False),
+                                       (torch.float8_e4m3fn, True)])
+def test_block_table_permutation_is_bit_exact(kv, decode):
+    extra = dict(seqs=[(1, 300), (1, 45), (2, 100)], num_q_heads=8, num_kv_heads=4) if decode else {}
+    spec = _small(7, kv_dtype=kv, window=100, sinks=True, num_blocks=80, **extra)
     inp = W.make(spec)
     base = run(inp, backend="split").cpu()
     perm = torch.randperm(inp.k_cache.shape[0], generator=torch.Generator().manual_seed(5))
