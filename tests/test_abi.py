@@ -89,8 +89,15 @@ def test_dispatcher_splits_long_underfilled_decode():
     p = _plan()
     assert p["path"] == _lib.UA_PATH_SPLIT and p["n_part"] >= 2
     assert p["block_m"] == 16 and p["grid_y"] == 8 and p["grid_z"] == p["n_part"]
-    assert p["grid_x"] == 8 and p["slot_per_seq"] == 1 and p["cluster_y"] == 8
-    assert p["workspace_bytes"] >= 8 * 32 * p["n_part"] * (128 + 2) * 4
+    assert p["grid_x"] == 8 and p["slot_per_seq"] == 1
+    # the partitions of a slot form one cluster with some of its kv-heads (8 CTAs at most)
+    # and merge through distributed shared memory: no workspace
+    assert p["cluster_z"] == p["n_part"] and p["cluster_y"] * p["cluster_z"] <= 8
+    assert 8 % p["cluster_y"] == 0 and p["workspace_bytes"] == 0
+    # more than 8 partitions: the merge kernel and its scratch
+    p = _plan(backend="split", num_splits=12)
+    assert p["cluster_z"] == 1 and p["cluster_y"] == 8
+    assert p["workspace_bytes"] >= 8 * 32 * 12 * (128 + 2) * 4
 
 
 def test_dispatcher_keeps_short_or_full_grids_on_2d():
@@ -105,7 +112,7 @@ def test_dispatcher_forced_backends_and_split_count():
     assert _plan(backend="2d")["n_part"] == 1
     assert _plan(backend="split", max_seqlen_k=40, window_left=-1)["n_part"] >= 2
     assert _plan(backend="split", num_splits=5)["n_part"] == 5
-    one = _plan(backend="split", num_splits=5)["workspace_bytes"]
+    one = _plan(backend="split", num_splits=12)["workspace_bytes"]
     assert one > 0
     assert ua._lib.load().ua_workspace_bytes is not None
 

@@ -52,6 +52,7 @@ class UaPlan(ctypes.Structure):
         ("grid_z", ctypes.c_int32),
         ("num_sms", ctypes.c_int32),
         ("cluster_y", ctypes.c_int32),
+        ("cluster_z", ctypes.c_int32),
         ("slot_per_seq", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_size_t),
     ]

@@ -190,10 +190,19 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
         cy = c;
         break;
       }
+  // Decode-shaped split: the partitions of a slot join the cluster (at most 8 CTAs, the
+  // portable size) and merge through distributed shared memory: no merge kernel, no
+  // workspace.
+  int cz = 1;
+  if (!tc && wm == 1 && n_part > 1 && n_part <= 8) {
+    cz = n_part;
+    while (cy * cz > 8) cy >>= 1;
+  }
   pl->cluster_y = cy;
+  pl->cluster_z = cz;
   pl->slot_per_seq = per_seq ? 1 : 0;
   pl->workspace_bytes = 0;
-  if (n_part > 1) {
+  if (n_part > 1 && cz == 1) {
     const size_t rows = static_cast<size_t>(sh->total_q) * hq * n_part;
     // m and l, then acc; each piece rounded to 256 bytes
     const size_t ml = ((rows * sizeof(float) + 255) / 256) * 256;
@@ -315,7 +324,8 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
     }
     pp.tq = 128 / group;
   }
-  if (pl.n_part > 1) {
+  p.cluster_merge = pl.cluster_z > 1 ? 1 : 0;
+  if (pl.n_part > 1 && !p.cluster_merge) {
     void* ws = sh->workspace;
     if (ws != nullptr) {
       if (sh->workspace_bytes < pl.workspace_bytes || !aligned16(ws)) return UA_ERR_WORKSPACE;
@@ -347,13 +357,13 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
       default: err = ua::launch_prefill_d256(pp, grid, kv, feat, nq, st); break;
     }
   } else switch (d) {
-    case 64: err = ua::launch_tile_d64(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
-    case 128: err = ua::launch_tile_d128(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
-    default: err = ua::launch_tile_d256(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, st); break;
+    case 64: err = ua::launch_tile_d64(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, pl.cluster_z, st); break;
+    case 128: err = ua::launch_tile_d128(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, pl.cluster_z, st); break;
+    default: err = ua::launch_tile_d256(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, pl.cluster_z, st); break;
   }
   if (err != cudaSuccess) return UA_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], st) != cudaSuccess) return UA_ERR_CUDA;
-  if (pl.n_part > 1) {
+  if (pl.n_part > 1 && !p.cluster_merge) {
     ua::MergeParams mp{};
     mp.ws_m = p.ws_m;
     mp.ws_l = p.ws_l;

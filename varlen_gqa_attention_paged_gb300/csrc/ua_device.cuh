@@ -120,11 +120,12 @@ __device__ __forceinline__ void grid_launch_dependents() {
 
 // Launch with programmatic stream serialisation (the kernel must call
 // grid_dependency_wait() before it touches memory the previous kernel writes), and,
-// with cluster_y > 1, as clusters of cluster_y CTAs along grid y that the hardware
-// schedules together.
+// with cluster_y or cluster_z > 1, as clusters of cluster_y x cluster_z CTAs along grid
+// y and z that the hardware schedules together.
 template <typename... Args, typename... Act>
-inline cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t stream, int cluster_y, Act&&... args) {
+inline cudaError_t launch_pdl_cluster(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t stream, int cluster_y, int cluster_z,
+                                      Act&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -134,16 +135,60 @@ inline cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   int n = 1;
-  if (cluster_y > 1) {
+  if (cluster_y > 1 || cluster_z > 1) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 1;
     attr[1].val.clusterDim.y = static_cast<unsigned>(cluster_y);
-    attr[1].val.clusterDim.z = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(cluster_z);
     n = 2;
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Act>(args)...);
+}
+
+template <typename... Args, typename... Act>
+inline cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, int cluster_y, Act&&... args) {
+  return launch_pdl_cluster(kern, grid, block, smem, stream, cluster_y, 1,
+                            std::forward<Act>(args)...);
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+
+// Cluster-wide barrier: every thread of every CTA of the cluster arrives; shared-memory
+// writes before it are visible to the cluster's CTAs after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctaid_y() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctaid.y;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctaid_y() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctaid.y;" : "=r"(r));
+  return r;
+}
+// The shared::cluster address of local shared address `a` in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
 }
 
 // ---------------------------------------------------------------- warp MMA (m16n8k16)

@@ -35,6 +35,8 @@ struct AttnParams {
   int hq, hkv, group;
   int qq_stride, window_left, n_part;
   int slot_per_seq;             // 1: grid slot x is sequence x (every sequence fits one q-block)
+  int cluster_merge;            // 1: the n_part partitions (grid z) of a slot form one cluster
+                                //    and merge through distributed shared memory
   int q_dtype, out_dtype;
   float scale, softcap;
 };
@@ -76,11 +78,11 @@ struct MergeParams {
 constexpr int tile_block_m(int wm) { return 16 * wm; }
 
 cudaError_t launch_tile_d64(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
-                            int cluster_y, cudaStream_t s);
+                            int cluster_y, int cluster_z, cudaStream_t s);
 cudaError_t launch_tile_d128(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
-                             int cluster_y, cudaStream_t s);
+                             int cluster_y, int cluster_z, cudaStream_t s);
 cudaError_t launch_tile_d256(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
-                             int cluster_y, cudaStream_t s);
+                             int cluster_y, int cluster_z, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_prefill_d64(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
                                cudaStream_t s);

@@ -81,12 +81,16 @@ struct TileCfg {
   // columns are put back in order when written.
   static constexpr bool kPermD = KV == KV_E4M3;
   static constexpr int kMergeBytes = (kWN > 1) ? kConsumerWarps * (2 * 16 + (D / 8) * 32 * 4) * 4 : 0;
+  // decode-shaped CTAs of one cluster exchange their partitions' rows (max, sum, D
+  // unnormalised outputs of 16 rows) through distributed shared memory
+  static constexpr int kPartBytes = (WM == 1) ? 16 * (D + 2) * 4 : 0;
   // decode-shaped CTAs aim at two per SM (about 110 KB each); the 64-row variant at one
   static constexpr int kBudget = (WM == 1 ? 110 : 200) * 1024;
   static constexpr int kStagesFit = kBudget / kStageBytes;
   static constexpr int kStages = kStagesFit < 2 ? 2 : (kStagesFit > 4 ? 4 : kStagesFit);
-  static constexpr int kPipeRaw =
-      (kStages * kStageBytes > kMergeBytes) ? kStages * kStageBytes : kMergeBytes;
+  static constexpr int kPipeRaw = (kStages * kStageBytes > kMergeBytes + kPartBytes)
+                                      ? kStages * kStageBytes
+                                      : kMergeBytes + kPartBytes;
   static constexpr int kPipeBytes = (kPipeRaw + 1023) & ~1023;
   static constexpr int kSmemBytes = 1024 + kPipeBytes + 2 * kStages * 8;
   // two CTAs per SM when they fit, but not at d256, whose 16 x 256 fp32 accumulators alone
@@ -341,6 +345,10 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
     // Never leave copies in flight into this CTA's shared memory.
     for (int t = max(0, issued - S); t < issued; ++t)
       mbar_wait_bounded(&full[t % S], (t / S) & 1, p.status, DEV_TIMEOUT);
+    if (WM == 1 && p.cluster_merge) {  // the consumers' two cluster barriers
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
 
@@ -664,11 +672,19 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
 
   if (aborted) s_abort = 1;
   named_bar_sync(1, 32 * C::kConsumerWarps);
-  if (s_abort) return;
+  // Split partitions of a decode-shaped q-block that form one cluster merge through
+  // distributed shared memory (every CTA reaches both cluster barriers, an aborted one
+  // too); otherwise an aborted CTA writes nothing.
+  const bool cmerge = WM == 1 && p.cluster_merge != 0;
+  if (s_abort && !cmerge) return;
+  const bool ok = s_abort == 0;
 
   const size_t n_part = static_cast<size_t>(p.n_part);
-  if constexpr (C::kWN == 1) {
-    // Each warp owns its 16 rows: write straight from registers.
+  float* const partial = reinterpret_cast<float*>(pipe + C::kMergeBytes);  // [16][D], m[16], l[16]
+  // Rows rr of the warp's fragments: the normalised output (one partition), the
+  // partition's max / sum / unnormalised output in the split scratch, or (cluster merge)
+  // in this CTA's shared memory.
+  auto write_rows = [&]() {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       if (!rv[rr]) continue;
@@ -678,6 +694,13 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
         const size_t esz = p.out_dtype == UA_DT_F32 ? 4 : 2;
         store_o_row<D, C::kPermD>(o_acc, rr, cq, inv, static_cast<uint8_t*>(p.out) + row * D * esz,
                                   p.out_dtype);
+      } else if (cmerge) {
+        const int pr = gq + 8 * rr;  // row within the q-block
+        if (cq == 0) {
+          partial[16 * D + pr] = m_run[rr];
+          partial[16 * D + 16 + pr] = l_run[rr];
+        }
+        store_o_row<D, C::kPermD>(o_acc, rr, cq, v_scale, partial + pr * D, UA_DT_F32);
       } else {
         const size_t w = row * n_part + z;
         if (cq == 0) {
@@ -687,6 +710,10 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
         store_o_row<D, C::kPermD>(o_acc, rr, cq, v_scale, p.ws_acc + w * D, UA_DT_F32);
       }
     }
+  };
+  if constexpr (C::kWN == 1) {
+    // Each warp owns its 16 rows: write straight from registers.
+    write_rows();
   } else {
     // Four warps hold the same 16 rows over different keys (the pipeline buffers are free:
     // every copy landed and every consumer is done).  Each warp rescales its state to the
@@ -726,43 +753,98 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
             make_float4(o_acc[nd][0], o_acc[nd][1], o_acc[nd][2], o_acc[nd][3]);
     }
     named_bar_sync(1, 32 * C::kConsumerWarps);
-    if (warp != 0) return;
+    if (warp == 0) {
 #pragma unroll
-    for (int w = 1; w < C::kConsumerWarps; ++w) {
-      l_run[0] += sm_l[w * 16 + gq];
-      l_run[1] += sm_l[w * 16 + gq + 8];
+      for (int w = 1; w < C::kConsumerWarps; ++w) {
+        l_run[0] += sm_l[w * 16 + gq];
+        l_run[1] += sm_l[w * 16 + gq + 8];
 #pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        const float4 o4 = sm_o[(w * (D / 8) + nd) * 32 + lane];
-        o_acc[nd][0] += o4.x;
-        o_acc[nd][1] += o4.y;
-        o_acc[nd][2] += o4.z;
-        o_acc[nd][3] += o4.w;
-      }
-    }
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      if (!rv[rr]) continue;
-      const size_t row = static_cast<size_t>(rt[rr]) * p.hq + rh[rr];
-      if (n_part == 1) {
-        const float inv = l_run[rr] > 0.f ? v_scale / l_run[rr] : 0.f;
-        const size_t esz = p.out_dtype == UA_DT_F32 ? 4 : 2;
-        store_o_row<D, C::kPermD>(o_acc, rr, cq, inv, static_cast<uint8_t*>(p.out) + row * D * esz,
-                                  p.out_dtype);
-      } else {
-        const size_t w = row * n_part + z;
-        if (cq == 0) {
-          p.ws_m[w] = m_run[rr];
-          p.ws_l[w] = l_run[rr];
+        for (int nd = 0; nd < D / 8; ++nd) {
+          const float4 o4 = sm_o[(w * (D / 8) + nd) * 32 + lane];
+          o_acc[nd][0] += o4.x;
+          o_acc[nd][1] += o4.y;
+          o_acc[nd][2] += o4.z;
+          o_acc[nd][3] += o4.w;
         }
-        store_o_row<D, C::kPermD>(o_acc, rr, cq, v_scale, p.ws_acc + w * D, UA_DT_F32);
+      }
+      if (ok) write_rows();
+    }
+  }
+  if (!cmerge) return;
+
+  // Cluster merge: the cluster is the n_part partitions (grid z) of cluster_y kv-heads of
+  // this q-block slot; partition zz of this kv-head is the cluster's CTA
+  // cluster_ctaid.y + cluster_y * zz.  Row r of the q-block is merged by partition
+  // r mod n_part, one warp a row (the LSE merge of the split path):
+  //   M = max_{l_z > 0} m_z,  L = sum l_z 2^(m_z - M),  out = sum acc_z 2^(m_z - M) / L.
+  cluster_sync();
+  {
+    constexpr int kPer = D / 32;
+    const int np = p.n_part;
+    const uint32_t cy = cluster_nctaid_y(), yc = cluster_ctaid_y();
+    const uint32_t part_s = smem_addr(partial);
+    const size_t esz = p.out_dtype == UA_DT_F32 ? 4 : 2;
+    for (int k = warp;; k += C::kConsumerWarps) {
+      const int r = z + np * k;  // row within the q-block
+      if (r >= r1 - r0) break;
+      const int tok = q0 + (r0 + r) / G;
+      if (tok >= p.total_q) break;
+      const size_t orow = static_cast<size_t>(tok) * p.hq + g * G + (r0 + r) % G;
+      float mz = -INFINITY, lz = 0.f;
+      if (lane < np) {
+        const uint32_t rank = yc + cy * lane;
+        mz = ld_cluster_f32(cluster_map(part_s + (16 * D + r) * 4, rank));
+        lz = ld_cluster_f32(cluster_map(part_s + (16 * D + 16 + r) * 4, rank));
+      }
+      float M = lz > 0.f ? mz : -INFINITY;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float wz = (lz > 0.f && M != -INFINITY) ? fast_exp2(mz - M) : 0.f;
+      float L = lz * wz;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      float acc[kPer];
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+      for (int zz = 0; zz < np; ++zz) {
+        const float wt = __shfl_sync(0xffffffffu, wz, zz);
+        if (wt == 0.f) continue;  // uniform: an empty partition
+        const uint32_t a = cluster_map(part_s + (r * D + lane * kPer) * 4, yc + cy * zz);
+#pragma unroll
+        for (int e = 0; e < kPer; e += 4) {
+          if constexpr (kPer >= 4) {
+            const float4 v = ld_cluster_f32x4(a + e * 4);
+            acc[e] += v.x * wt;
+            acc[e + 1] += v.y * wt;
+            acc[e + 2] += v.z * wt;
+            acc[e + 3] += v.w * wt;
+          } else {
+#pragma unroll
+            for (int f = 0; f < kPer; ++f) acc[f] += ld_cluster_f32(a + f * 4) * wt;
+          }
+        }
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      uint8_t* dst = static_cast<uint8_t*>(p.out) + orow * D * esz;
+#pragma unroll
+      for (int e = 0; e < kPer; e += 2) {
+        const int col = lane * kPer + e;
+        const float x0 = acc[e] * inv, x1 = acc[e + 1] * inv;
+        if (p.out_dtype == UA_DT_F32) {
+          *reinterpret_cast<float2*>(reinterpret_cast<float*>(dst) + col) = make_float2(x0, x1);
+        } else {
+          const uint32_t v = p.out_dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
+          *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(dst) + col) = v;
+        }
       }
     }
   }
+  cluster_sync();  // no CTA leaves while the cluster still reads its shared memory
 }
 
 template <int D, int KV, int WM, bool FEAT, bool TMA>
-cudaError_t launch_tile_t(const TileParams& tp, dim3 grid, int cluster_y, cudaStream_t stream) {
+cudaError_t launch_tile_t(const TileParams& tp, dim3 grid, int cluster_y, int cluster_z,
+                          cudaStream_t stream) {
   using C = TileCfg<D, KV, WM>;
   auto kern = ua_attn_tile_kernel<D, KV, WM, FEAT, TMA>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
@@ -775,19 +857,20 @@ cudaError_t launch_tile_t(const TileParams& tp, dim3 grid, int cluster_y, cudaSt
     if (err != cudaSuccess) return err;
     configured.fetch_or(bit);
   }
-  return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, cluster_y, tp);
+  return launch_pdl_cluster(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, cluster_y,
+                            cluster_z, tp);
 }
 
 template <int D>
 cudaError_t launch_tile_dispatch(const TileParams& tp, dim3 grid, int wm, int kv, bool feat,
-                                 bool tma, int cluster_y, cudaStream_t s) {
+                                 bool tma, int cluster_y, int cluster_z, cudaStream_t s) {
 #define UA_TILE_CASE(KVV, WMV)                                                        \
   if (kv == KVV && wm == WMV) {                                                       \
     if (tma)                                                                          \
-      return feat ? launch_tile_t<D, KVV, WMV, true, true>(tp, grid, cluster_y, s)    \
-                  : launch_tile_t<D, KVV, WMV, false, true>(tp, grid, cluster_y, s);  \
-    return feat ? launch_tile_t<D, KVV, WMV, true, false>(tp, grid, cluster_y, s)     \
-                : launch_tile_t<D, KVV, WMV, false, false>(tp, grid, cluster_y, s);   \
+      return feat ? launch_tile_t<D, KVV, WMV, true, true>(tp, grid, cluster_y, cluster_z, s)    \
+                  : launch_tile_t<D, KVV, WMV, false, true>(tp, grid, cluster_y, cluster_z, s);  \
+    return feat ? launch_tile_t<D, KVV, WMV, true, false>(tp, grid, cluster_y, cluster_z, s)     \
+                : launch_tile_t<D, KVV, WMV, false, false>(tp, grid, cluster_y, cluster_z, s);   \
   }
   UA_TILE_CASE(KV_F16, 1)
   UA_TILE_CASE(KV_F16, 4)
