@@ -217,7 +217,9 @@ class Call:
                      float(inp.scale), float(inp.softcap), int(inp.window_left),
                      p(self.d["alibi_slopes"]), p(self.d["qq_bias"]), p(self.d["sinks"]),
                      ua._DTYPES[spec.kv_dtype], p(self.kv_scale), self.backend]
-        self.launches_per_call = 2 if self.plan["path"] == ua.UA_PATH_SPLIT else 1
+        # the split path merges in a second kernel unless its partitions merge in-cluster
+        self.launches_per_call = (2 if self.plan["path"] == ua.UA_PATH_SPLIT and
+                                  self.plan["cluster_z"] <= 1 else 1)
 
     def __call__(self, stream, replica=0, events=None):
         if events is not None:
@@ -253,11 +255,13 @@ def n_replicas(spec):
 
 
 def measure_workload(spec, dev, stream, steps, warmup, backend="auto"):
-    """Device time per call (library events around each kernel), median over calls."""
+    """Device time per call (library events around each kernel, median over calls) and the
+    average step of the same calls back to back (events around the whole loop only)."""
     reps = n_replicas(spec)
     inp = W.make(spec, replicas=reps)
     call = Call(inp, dev, backend=backend)
     evs, arrs = event_triplets(steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for i in range(warmup):
             call(stream, replica=i)
@@ -265,25 +269,35 @@ def measure_workload(spec, dev, stream, steps, warmup, backend="auto"):
         for i in range(steps):
             call(stream, replica=i, events=arrs[i])
         torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(steps):
+            call(stream, replica=i)
+        e1.record(stream)
+        torch.cuda.synchronize()
     attn = [evs[i][0].elapsed_time(evs[i][1]) for i in range(steps)]
     total = [evs[i][0].elapsed_time(evs[i][2]) for i in range(steps)]
-    return inp, call, reps, attn, total
+    return inp, call, reps, attn, total, e0.elapsed_time(e1) / steps
 
 
-def workload_record(inp, call, reps, attn_ms, total_ms, hbm_peak, tc_peak):
+def workload_record(inp, call, reps, attn_ms, total_ms, step_ms, hbm_peak, tc_peak):
+    """us_per_call: one call alone (events around it); step_us: the same calls back to back.
+    The kernel time behind the roofline fractions is the back-to-back step where a call is
+    one kernel launch, else the attention kernel's own events."""
     spec = inp.spec
     med = statistics.median(total_ms)
     kbytes = W.kv_bytes_read(inp)
     flops = W.attention_flops(inp)
+    kern_ms = step_ms if call.launches_per_call == 1 else statistics.median(attn_ms)
     rec = {"kernel": kernel_name(call.plan, spec.head_dim),
            "path": "split" if call.plan["path"] == 2 else "2d", "n_part": call.plan["n_part"],
-           "kernel_block_m": call.plan["block_m"], "us_per_call": round(med * 1e3, 2),
-           "attn_kernel_us": round(statistics.median(attn_ms) * 1e3, 2),
-           "tokens_per_s": round(inp.total_q / (med * 1e-3), 1),
-           "kv_gbs": round(kbytes / (med * 1e-3) / 1e9, 1),
-           "hbm_frac": round(kbytes / (statistics.median(attn_ms) * 1e-3) / 1e9 / hbm_peak, 4),
-           "tflops": round(flops / (med * 1e-3) / 1e12, 2),
-           "tensor_frac": round(flops / (statistics.median(attn_ms) * 1e-3) / 1e12 / tc_peak, 4),
+           "kernel_block_m": call.plan["block_m"], "launches_per_call": call.launches_per_call,
+           "us_per_call": round(med * 1e3, 2), "step_us": round(step_ms * 1e3, 2),
+           "attn_kernel_us": round(kern_ms * 1e3, 2),
+           "tokens_per_s": round(inp.total_q / (step_ms * 1e-3), 1),
+           "kv_gbs": round(kbytes / (step_ms * 1e-3) / 1e9, 1),
+           "hbm_frac": round(kbytes / (kern_ms * 1e-3) / 1e9 / hbm_peak, 4),
+           "tflops": round(flops / (step_ms * 1e-3) / 1e12, 2),
+           "tensor_frac": round(flops / (kern_ms * 1e-3) / 1e12 / tc_peak, 4),
            "l2": f"{reps} cache replicas rotated"}
     return rec
 
@@ -379,9 +393,9 @@ def run_ours(args):
             if not name or name == args.workload:
                 continue
             try:
-                w_inp, w_call, w_reps, a_ms, t_ms = measure_workload(
+                w_inp, w_call, w_reps, a_ms, t_ms, s_ms = measure_workload(
                     W.WORKLOADS[name], dev, stream, steps=args.workload_steps, warmup=3)
-                extra[name] = workload_record(w_inp, w_call, w_reps, a_ms, t_ms, hbm_peak,
+                extra[name] = workload_record(w_inp, w_call, w_reps, a_ms, t_ms, s_ms, hbm_peak,
                                               tc_burst)
                 del w_inp, w_call
                 torch.cuda.empty_cache()
@@ -392,7 +406,11 @@ def run_ours(args):
         return
     tokens_per_step = inp.total_q
     value = job_throughput(tokens_per_step, args.steps, elapsed_ms, world)
-    attn_us = statistics.mean(attn_ms) * 1e3
+    # One kernel launch per step: its average duration is the timed region over K steps
+    # (launch gaps included).  Two (partition + merge kernel): the partition kernel's own
+    # events in the pass after the timed region.
+    one_launch = call.launches_per_call == 1
+    attn_us = elapsed_ms / args.steps * 1e3 if one_launch else statistics.mean(attn_ms) * 1e3
     kbytes = W.kv_bytes_read(inp)
     flops = W.attention_flops(inp)
     kname = kernel_name(call.plan, spec.head_dim)
@@ -433,9 +451,14 @@ def run_ours(args):
                      "traffic": recorded_traffic(kname, spec.name), "peak_source": peak_kind,
                      "kernel": kname + (" (split-KV partition)" if call.plan["path"] == 2 else ""),
                      "kernel_us_mean": round(attn_us, 3),
-                     "kernel_timing": "CUDA events around the attention kernel, every step of "
-                                      "a pass of the same K steps right after the timed region",
-                     "merge_us_mean": round(statistics.mean(merge_ms) * 1e3, 3)},
+                     "kernel_timing": (
+                         "CUDA events around the K timed steps on the launching stream, one "
+                         "kernel launch a step (split partitions merged in-cluster): timed "
+                         "region / K, launch gaps included" if one_launch else
+                         "CUDA events around the attention kernel, every step of a pass of "
+                         "the same K steps right after the timed region"),
+                     "merge_us_mean": None if one_launch else
+                     round(statistics.mean(merge_ms) * 1e3, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * tokens_per_step * e2e_steps / (e2e_ms * 1e-3), 1),
                 "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

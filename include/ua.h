@@ -119,8 +119,8 @@ typedef struct {
   int32_t num_sms;     /* SM count the plan was made for */
   int32_t cluster_y;   /* CTAs of one q-block slot (different kv-heads) launched as a cluster */
   int32_t cluster_z;   /* > 1: the n_part partitions of a slot are one cluster too (cluster
-                          cluster_y x cluster_z) and merge through distributed shared memory,
-                          with no merge kernel and no workspace */
+                          cluster_y x cluster_z, at most 16 CTAs) and merge through
+                          distributed shared memory, with no merge kernel and no workspace */
   int32_t slot_per_seq; /* 1: every sequence fits one q-block and grid slot x is sequence x */
   size_t workspace_bytes; /* scratch the split path needs (0 on the 2D path) */
 } ua_plan_t;

@@ -94,10 +94,13 @@ def test_dispatcher_splits_long_underfilled_decode():
     # and merge through distributed shared memory: no workspace
     assert p["cluster_z"] == p["n_part"] and p["cluster_y"] * p["cluster_z"] <= 8
     assert 8 % p["cluster_y"] == 0 and p["workspace_bytes"] == 0
-    # more than 8 partitions: the merge kernel and its scratch
+    # 9 to 16 partitions: a cluster of the partitions alone
     p = _plan(backend="split", num_splits=12)
+    assert p["cluster_z"] == 12 and p["cluster_y"] == 1 and p["workspace_bytes"] == 0
+    # more than 16 partitions: the merge kernel and its scratch
+    p = _plan(backend="split", num_splits=20)
     assert p["cluster_z"] == 1 and p["cluster_y"] == 8
-    assert p["workspace_bytes"] >= 8 * 32 * 12 * (128 + 2) * 4
+    assert p["workspace_bytes"] >= 8 * 32 * 20 * (128 + 2) * 4
 
 
 def test_dispatcher_keeps_short_or_full_grids_on_2d():
@@ -112,7 +115,7 @@ def test_dispatcher_forced_backends_and_split_count():
     assert _plan(backend="2d")["n_part"] == 1
     assert _plan(backend="split", max_seqlen_k=40, window_left=-1)["n_part"] >= 2
     assert _plan(backend="split", num_splits=5)["n_part"] == 5
-    one = _plan(backend="split", num_splits=12)["workspace_bytes"]
+    one = _plan(backend="split", num_splits=20)["workspace_bytes"]
     assert one > 0
     assert ua._lib.load().ua_workspace_bytes is not None
 

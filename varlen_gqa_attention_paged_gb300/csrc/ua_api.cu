@@ -190,13 +190,13 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
         cy = c;
         break;
       }
-  // Decode-shaped split: the partitions of a slot join the cluster (at most 8 CTAs, the
-  // portable size) and merge through distributed shared memory: no merge kernel, no
-  // workspace.
+  // Decode-shaped split: the partitions of a slot join the cluster (8 CTAs at most, the
+  // portable size; up to 16 partitions alone in a cluster of up to 16) and merge through
+  // distributed shared memory: no merge kernel, no workspace.
   int cz = 1;
-  if (!tc && wm == 1 && n_part > 1 && n_part <= 8) {
+  if (!tc && wm == 1 && n_part > 1 && n_part <= 16) {
     cz = n_part;
-    while (cy * cz > 8) cy >>= 1;
+    while (cy * cz > (cz > 8 ? 16 : 8)) cy >>= 1;
   }
   pl->cluster_y = cy;
   pl->cluster_z = cz;

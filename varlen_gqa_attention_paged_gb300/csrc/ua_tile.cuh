@@ -855,6 +855,9 @@ cudaError_t launch_tile_t(const TileParams& tp, dim3 grid, int cluster_y, int cl
   if (!(configured.load() & bit)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
+    // clusters of up to 16 CTAs (the partitions of a decode slot)
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
     configured.fetch_or(bit);
   }
   return launch_pdl_cluster(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, cluster_y,
