@@ -53,6 +53,8 @@ def peaks():
 # only while these are unchanged).
 KERNEL_SOURCES = {
     "ua_attn_tile_kernel": ["ua_tile.cuh", "ua_tile_d*.cu", "ua_device.cuh", "ua_internal.h"],
+    "ua_decode_kernel": ["ua_decode.cuh", "ua_decode_d*.cu", "ua_tile.cuh", "ua_device.cuh",
+                         "ua_internal.h"],
     "ua_prefill_tm_kernel": ["ua_prefill_tm.cuh", "ua_prefill.cuh", "ua_prefill_d64.cu",
                              "ua_prefill_d128.cu", "ua_device.cuh", "ua_internal.h"],
     "ua_prefill_wide_kernel": ["ua_prefill_wide.cuh", "ua_prefill.cuh", "ua_prefill_d256.cu",
@@ -74,6 +76,8 @@ def kernel_name(plan, head_dim):
     """The attention kernel a plan launches."""
     if plan["kernel"] in (8, 16):
         return "ua_prefill_tm_kernel" if head_dim <= 128 else "ua_prefill_wide_kernel"
+    if plan["kernel"] == 2:
+        return "ua_decode_kernel"
     return "ua_attn_tile_kernel"
 
 
@@ -429,7 +433,7 @@ def run_ours(args):
     kbytes = W.kv_bytes_read(inp)
     flops = W.attention_flops(inp)
     kname = kernel_name(call.plan, spec.head_dim)
-    if kname == "ua_attn_tile_kernel":  # bandwidth-bound: algorithmic K/V bytes
+    if kname in ("ua_attn_tile_kernel", "ua_decode_kernel"):  # bandwidth-bound: K/V bytes
         achieved = kbytes / (attn_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "algorithmic_bytes_per_launch": kbytes}

@@ -106,6 +106,8 @@ typedef struct {
 typedef struct {
   int32_t path;        /* ua_path_t */
   int32_t kernel;      /* 1: warp-MMA tile kernel, 16 rows per CTA (decode-shaped q-blocks);
+                          2: key-major decode tile, 8 rows per CTA (decode with at most 8
+                          rows per kv-head, head_dim <= 128, 16 | block_size);
                           4: warp-MMA tile kernel, 64 rows per CTA (fp8 caches, block sizes
                           not a multiple of 16); 8: tensor-memory (tcgen05) kernel with
                           128-row q-blocks of floor(128 / G) tokens x G heads; 16: the same

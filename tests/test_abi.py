@@ -88,7 +88,9 @@ def _plan(**kw):
 def test_dispatcher_splits_long_underfilled_decode():
     p = _plan()
     assert p["path"] == _lib.UA_PATH_SPLIT and p["n_part"] >= 2
-    assert p["block_m"] == 16 and p["grid_y"] == 8 and p["grid_z"] == p["n_part"]
+    # the key-major decode tile: 8 rows of a kv-head per CTA, three CTAs per SM
+    assert p["kernel"] == 2 and p["block_m"] == 8
+    assert p["grid_y"] == 8 and p["grid_z"] == p["n_part"]
     assert p["grid_x"] == 8 and p["slot_per_seq"] == 1
     # the partitions of a slot form one cluster with some of its kv-heads (8 CTAs at most)
     # and merge through distributed shared memory: no workspace
@@ -130,10 +132,22 @@ def test_dispatcher_split_fits_one_wave():
         p = _plan(num_seqs=seqs, total_q=seqs, num_kv_heads=hkv, num_q_heads=4 * hkv, kv_dtype=kv,
                   window_left=-1, max_seqlen_k=100000)
         active = seqs * p["grid_y"]                     # CTAs of one partition
+        per_sm = 3 if p["kernel"] == 2 else 2           # the decode tile fits three an SM
         assert p["path"] == _lib.UA_PATH_SPLIT
-        assert active * p["n_part"] <= 2 * 152            # two CTAs per SM at most
-        # the largest count that fits: one more partition would start a second wave
-        assert active * (p["n_part"] + 1) > 2 * 152 or p["n_part"] == 128
+        assert active * p["n_part"] <= per_sm * 152
+        # the largest count that fits: one more partition would start a second wave (of
+        # the slots, or of the clusters, which host-only plans give 90 % of the slots)
+        assert active * (p["n_part"] + 1) > 0.9 * per_sm * 152 or p["n_part"] == 128
+
+
+def test_dispatcher_decode_kernels():
+    # at most 8 rows per kv-head, head_dim <= 128, page boxes: the key-major decode tile
+    assert _plan()["kernel"] == 2
+    assert _plan(head_dim=64, kv_dtype=2)["kernel"] == 2
+    # more rows (up to 16), head_dim 256, pages not a multiple of 16: the 16-row tile
+    assert _plan(max_seqlen_q=3)["kernel"] == 1
+    assert _plan(head_dim=256)["kernel"] == 1
+    assert _plan(block_size=13)["kernel"] == 1
 
 
 def test_dispatcher_mixed_batch_splits_underfilled_long_walks():

@@ -128,20 +128,26 @@ int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, in
 // then into as many partitions as still fit in that one wave (at least two): a
 // second, partly filled wave costs more than the extra parallelism gives back.
 //
-// Kernel: decode-shaped calls (every sequence's rows fit 16) take the warp-MMA tile kernel
-// with 16-row q-blocks; other calls on fp16/bf16 caches with 16 | block_size take the
+// Kernel: decode calls with at most 8 rows per kv-head, head_dim <= 128 and page-sized
+// TMA boxes take the key-major decode tile (keys on the MMA's M side, rows on N); other
+// decode-shaped calls (every sequence's rows fit 16) take the warp-MMA tile kernel with
+// 16-row q-blocks; other calls on fp16/bf16 caches with 16 | block_size take the
 // tensor-memory kernel with 128-row q tiles (floor(128 / G) tokens x G heads), two tiles
 // per CTA for head_dim <= 128 when that grid still fills the device; the rest (fp8
 // caches, other block sizes) take the tile kernel with 64-row q-blocks.
 bool is_tc(int kernel) { return kernel == ua::KERNEL_TC128 || kernel == ua::KERNEL_TC256; }
 
 void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int window_left,
-               int kv_dtype, int backend, int num_sms, bool allow_tc, ua_plan_t* pl) {
+               int kv_dtype, int backend, int num_sms, bool allow_tc, bool allow_dec,
+               bool query_device, ua_plan_t* pl) {
   const int group = hq / hkv;
   const long long rows_max = static_cast<long long>(sh->max_seqlen_q) * group;
   const bool tc = allow_tc && rows_max > 16 && group <= 128 && block_size % 16 == 0 &&
                   (kv_dtype == UA_DT_F16 || kv_dtype == UA_DT_BF16);
-  const int wm = rows_max <= 16 ? 1 : 4;
+  // decode with at most 8 rows per kv-head: the key-major decode tile (page boxes)
+  const bool dec = allow_dec && !tc && rows_max <= 8 && d <= 128 && block_size % 16 == 0 &&
+                   static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
+  const int wm = dec ? ua::KERNEL_DEC8 : rows_max <= 16 ? 1 : 4;
   const int tq = tc ? 128 / group : 0;               // tokens per 128-row tensor-memory tile
   // two tiles per CTA (sharing every K/V tile) where their tensor memory fits and the
   // grid still fills the device
@@ -163,16 +169,57 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
   if (window_left >= 0)
     walk = std::min<long long>(walk, static_cast<long long>(window_left) + 1 + (bm + group - 1) / group);
   const long long wave =
-      static_cast<long long>(num_sms) * (tc ? 1 : ua::tile_ctas_per_sm(d, kv_dtype, wm));
+      static_cast<long long>(num_sms) *
+      (tc ? 1 : dec ? ua::decode_ctas_per_sm(d, kv_dtype) : ua::tile_ctas_per_sm(d, kv_dtype, wm));
   const long long by_walk = std::max<long long>(1, walk / kMinPartitionKeys);
   const long long fit = std::max<long long>(2, std::min(wave / base, by_walk));
   int n_part = 1;
+  bool fitted = false;  // n_part chosen here rather than by the caller
   if (backend == UA_BACKEND_SPLIT) {
     n_part = sh->num_splits > 0 ? sh->num_splits : static_cast<int>(fit);
+    fitted = sh->num_splits <= 0;
   } else if (backend == UA_BACKEND_AUTO) {
-    if (base < wave && walk >= 2LL * kMinPartitionKeys) n_part = static_cast<int>(fit);
+    if (base < wave && walk >= 2LL * kMinPartitionKeys) {
+      n_part = static_cast<int>(fit);
+      fitted = true;
+    }
   }
   n_part = std::min(n_part, kMaxPartitions);
+  // Decode-shaped CTAs of one slot read the same cache pages for different kv-heads and
+  // are launched as one cluster (cluster_y kv-heads) so they are scheduled together; a
+  // split's partitions join that cluster (cluster_z = n_part; at most 8 CTAs, the portable
+  // size, or up to 16 partitions alone) and merge through distributed shared memory: no
+  // merge kernel, no workspace.
+  auto cluster_shape = [&](int np, int& cy, int& cz) {
+    cy = 1;
+    if (!tc && wm != 4)
+      for (int c = 8; c > 1; c >>= 1)
+        if (hkv % c == 0) {
+          cy = c;
+          break;
+        }
+    cz = 1;
+    if (!tc && wm != 4 && np > 1 && np <= 16) {
+      cz = np;
+      while (cy * cz > (cz > 8 ? 16 : 8)) cy >>= 1;
+    }
+  };
+  // A cluster's CTAs must be resident together, inside one GPU processing cluster, which
+  // leaves fewer co-resident CTAs than the SMs' slots; a fitted partition count shrinks
+  // until every cluster of the grid fits one wave (the decode tile asks the device; else
+  // 90 % of the slots for clusters of three CTAs or more).
+  if (fitted && !tc && wm != 4) {
+    for (; n_part > 2; --n_part) {
+      int cy, cz;
+      cluster_shape(n_part, cy, cz);
+      const int c = cy * cz;
+      if (c <= 1) break;
+      long long cap = -1;
+      if (dec && query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, cy, cz);
+      if (cap < 0) cap = c <= 2 ? wave / c : (wave * 9 / 10) / c;
+      if (slots * (hkv / cy) <= cap) break;
+    }
+  }
   pl->path = n_part > 1 ? UA_PATH_SPLIT : UA_PATH_2D;
   pl->kernel = tc ? (nq == 2 ? ua::KERNEL_TC256 : ua::KERNEL_TC128) : wm;
   pl->block_m = bm;
@@ -181,23 +228,8 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
   pl->grid_y = hkv;
   pl->grid_z = n_part;
   pl->num_sms = num_sms;
-  // decode-shaped CTAs of one slot read the same cache pages for different kv-heads:
-  // launch them as one cluster so they are scheduled together
-  int cy = 1;
-  if (!tc && wm == 1)
-    for (int c = 8; c > 1; c >>= 1)
-      if (hkv % c == 0) {
-        cy = c;
-        break;
-      }
-  // Decode-shaped split: the partitions of a slot join the cluster (8 CTAs at most, the
-  // portable size; up to 16 partitions alone in a cluster of up to 16) and merge through
-  // distributed shared memory: no merge kernel, no workspace.
-  int cz = 1;
-  if (!tc && wm == 1 && n_part > 1 && n_part <= 16) {
-    cz = n_part;
-    while (cy * cz > (cz > 8 ? 16 : 8)) cy >>= 1;
-  }
+  int cy, cz;
+  cluster_shape(n_part, cy, cz);
   pl->cluster_y = cy;
   pl->cluster_z = cz;
   pl->slot_per_seq = per_seq ? 1 : 0;
@@ -270,7 +302,8 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   int num_sms = 0;
   if ((rc = device_sm_count(&num_sms)) != UA_OK) return rc;
   ua_plan_t pl;
-  make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, true, &pl);
+  make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, true, true, true,
+            &pl);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   ua::TileParams tp{};
@@ -319,10 +352,23 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
         encode_cache_map(&pp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
         encode_cache_map(&pp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d);
     if (!maps) {
-      make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, false, &pl);
+      make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, false, true,
+                true, &pl);
       p.n_part = pl.n_part;
     }
     pp.tq = 128 / group;
+  }
+  // Page-sized TMA boxes need 16 | block_size and row coordinates that fit in int32; the
+  // decode tile needs them, else the call is planned again for the tile kernel.
+  bool tma = !is_tc(pl.kernel) && block_size % 16 == 0 &&
+             static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
+  if (tma)
+    tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
+          encode_cache_map(&tp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d);
+  if (pl.kernel == ua::KERNEL_DEC8 && !tma) {
+    make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, false, false,
+              true, &pl);
+    p.n_part = pl.n_part;
   }
   p.cluster_merge = pl.cluster_z > 1 ? 1 : 0;
   if (pl.n_part > 1 && !p.cluster_merge) {
@@ -339,12 +385,6 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
     p.ws_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ml);
   }
   const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
-  // Page-sized TMA boxes need 16 | block_size and row coordinates that fit in int32.
-  bool tma = !is_tc(pl.kernel) && block_size % 16 == 0 &&
-             static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
-  if (tma)
-    tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
-          encode_cache_map(&tp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d);
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(sh->events);
   if (ev && cudaEventRecord(ev[0], st) != cudaSuccess) return UA_ERR_CUDA;
   cudaError_t err;
@@ -356,6 +396,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
       case 128: err = ua::launch_prefill_d128(pp, grid, kv, feat, nq, st); break;
       default: err = ua::launch_prefill_d256(pp, grid, kv, feat, nq, st); break;
     }
+  } else if (pl.kernel == ua::KERNEL_DEC8) {
+    err = d == 64 ? ua::launch_decode_d64(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st)
+                  : ua::launch_decode_d128(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st);
   } else switch (d) {
     case 64: err = ua::launch_tile_d64(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, pl.cluster_z, st); break;
     case 128: err = ua::launch_tile_d128(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, pl.cluster_z, st); break;
@@ -406,9 +449,10 @@ int ua_plan(const ua_shape_t* shape, int block_size, int num_q_heads, int num_kv
     if (plan == nullptr) return UA_ERR_INVALID_ARG;
     int rc = check_sizes(shape, block_size, num_q_heads, num_kv_heads, head_dim, kv_dtype, backend);
     if (rc != UA_OK) return rc;
-    if (num_sms <= 0 && (rc = device_sm_count(&num_sms)) != UA_OK) return rc;
+    const bool on_device = num_sms <= 0;  // plan for this device (else host-only sizes)
+    if (on_device && (rc = device_sm_count(&num_sms)) != UA_OK) return rc;
     make_plan(shape, block_size, num_q_heads, num_kv_heads, head_dim, window_left, kv_dtype,
-              backend, num_sms, true, plan);
+              backend, num_sms, true, true, on_device, plan);
     return UA_OK;
   } catch (...) {
     return UA_ERR_CUDA;

@@ -75,7 +75,8 @@ struct MergeParams {
 };
 
 // Rows (query token x head of one kv group) per CTA of the tile kernel.
-constexpr int tile_block_m(int wm) { return 16 * wm; }
+// rows of one q-block (kernel 2, the key-major decode tile: 8)
+constexpr int tile_block_m(int wm) { return wm == 2 ? 8 : 16 * wm; }
 
 cudaError_t launch_tile_d64(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
                             int cluster_y, int cluster_z, cudaStream_t s);
@@ -83,6 +84,14 @@ cudaError_t launch_tile_d128(const TileParams& tp, dim3 grid, int wm, int kv, bo
                              int cluster_y, int cluster_z, cudaStream_t s);
 cudaError_t launch_tile_d256(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
                              int cluster_y, int cluster_z, cudaStream_t s);
+// key-major decode tile (head_dim 64, 128; TMA page boxes; at most 8 rows per kv-head)
+cudaError_t launch_decode_d64(const TileParams& tp, dim3 grid, int kv, bool feat, int cluster_y,
+                              int cluster_z, cudaStream_t s);
+cudaError_t launch_decode_d128(const TileParams& tp, dim3 grid, int kv, bool feat, int cluster_y,
+                               int cluster_z, cudaStream_t s);
+int decode_ctas_per_sm(int head_dim, int kv);
+// co-resident clusters of cluster_y x cluster_z decode CTAs on the current device (-1: unknown)
+int decode_cluster_capacity(int head_dim, int kv, int cluster_y, int cluster_z);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_prefill_d64(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
                                cudaStream_t s);
@@ -92,7 +101,7 @@ cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool
                                cudaStream_t s);
 
 // Plan kernel codes.
-enum : int { KERNEL_TILE16 = 1, KERNEL_TILE64 = 4, KERNEL_TC128 = 8, KERNEL_TC256 = 16 };
+enum : int { KERNEL_TILE16 = 1, KERNEL_DEC8 = 2, KERNEL_TILE64 = 4, KERNEL_TC128 = 8, KERNEL_TC256 = 16 };
 
 // Resident CTAs per SM of the tile kernel variant for (head_dim, kv dtype, wm).
 int tile_ctas_per_sm(int head_dim, int kv, int wm);
