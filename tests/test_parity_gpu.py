@@ -133,6 +133,13 @@ SMALL = {
                                  kv_dtype=torch.bfloat16, window=200, sinks=True),
     "dec_f16_d64_g8": dict(seqs=[(1, 500), (1, 31), (1, 16)], num_q_heads=16, num_kv_heads=2,
                             head_dim=64, block_size=32),
+    # 9 to 16 rows per kv-head, and head_dim 256: the 16-row tile kernel's decode path
+    "tile16_bf16_g8_q2": dict(seqs=[(2, 700), (1, 300), (2, 45), (1, 1)], num_q_heads=16,
+                              num_kv_heads=2, q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16,
+                              window=300, sinks=True),
+    "tile16_fp8_d256": dict(seqs=[(1, 900), (2, 260), (1, 3)], num_q_heads=12, num_kv_heads=2,
+                            head_dim=256, kv_dtype=torch.float8_e4m3fn, softcap=30.0,
+                            alibi=True),
 }
 
 
