@@ -252,6 +252,48 @@ def test_cluster_merge_partition_counts():
             assert max_err(got, want) <= TOL[spec.kv_dtype], (spec.name, n_part)
 
 
+@pytest.mark.parametrize("spec,kw", [(W.SWDECODE_BF16, {}),
+                                     (W.SWDECODE_FP8, dict(backend="split", num_splits=20)),
+                                     (W.MIXED, {})],
+                         ids=["cluster-merge", "merge-kernel-workspace", "tensor-memory-split"])
+def test_cuda_graph_capture_and_replay(spec, kw):
+    """A call captured in a CUDA graph replays with new inputs copied into the captured
+    buffers (after one warm-up call has configured the kernels and sized the library's
+    workspace): the in-cluster merge, the merge kernel over the library workspace, and
+    the tensor-memory kernel's split."""
+    inp = W.make(spec, poison=True, replicas=2)
+    d = to_dev(inp)
+    bt = d["block_table"][0].clone()
+    q = d["q"].clone()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def call():
+        ua.unified_attention(q, d["k_cache"], d["v_cache"], d["cu_seqlens_q"], d["seq_lens_k"],
+                             bt, max_seqlen_q=inp.max_seqlen_q, max_seqlen_k=inp.max_seqlen_k,
+                             scale=inp.scale, softcap=inp.softcap, window_left=inp.window_left,
+                             alibi_slopes=d["alibi_slopes"], qq_bias=d["qq_bias"],
+                             sinks=d["sinks"], kv_scale=d["kv_scale"], out=out, stream=stream,
+                             **kw)
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    for replica, qmul in ((1, 0.5), (0, 1.0)):
+        bt.copy_(d["block_table"][replica])
+        q.copy_(d["q"] * qmul)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        kwargs = inp.oracle_kwargs(replica)
+        kwargs["q"] = inp.q * qmul
+        want = oracle.attention(threads=THREADS, **kwargs)
+        assert max_err(out, want) <= TOL[spec.kv_dtype], (spec.name, replica)
+
+
 def test_out_of_range_block_id_is_reported_not_read():
     inp = W.make(_small(9))
     bt = inp.block_table.clone()
