@@ -67,6 +67,10 @@ class Problem(ctypes.Structure):
         ("softcap", ctypes.c_double),
         ("k_scale", ctypes.c_double),
         ("v_scale", ctypes.c_double),
+        ("k_scale_tok", ctypes.c_void_p),
+        ("v_scale_tok", ctypes.c_void_p),
+        ("k_scale_strides", ctypes.c_int64 * 3),
+        ("v_scale_strides", ctypes.c_int64 * 3),
     ]
 
 
@@ -130,9 +134,32 @@ def _opt_f32(x):
     return np.ascontiguousarray(a, dtype=np.float32)
 
 
+def _tok_scale(x):
+    """A per-token fp8 scale array [num_blocks, block_size, H_kv] (float32 numpy array or
+    torch tensor, any strides): the array kept alive, its first element's address and its
+    element strides."""
+    if x is None:
+        return None, None, (0, 0, 0)
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        torch = None
+    if torch is not None and isinstance(x, torch.Tensor):
+        if x.dtype != torch.float32:
+            raise TypeError("per-token scales must be float32")
+        a = x.detach().cpu().numpy()
+    else:
+        a = np.asarray(x)
+        if a.dtype != np.float32:
+            raise TypeError("per-token scales must be float32")
+    if a.ndim != 3 or any(st % 4 for st in a.strides) or any(st < 0 for st in a.strides):
+        raise ValueError("per-token scales are [num_blocks, block_size, H_kv] with positive strides")
+    return a, a.ctypes.data, tuple(st // 4 for st in a.strides)
+
+
 def _problem(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *, scale, softcap,
              window_left, alibi_slopes, qq_bias, qq_bias_stride, sinks, k_scale, v_scale,
-             q_dtype, kv_dtype):
+             q_dtype, kv_dtype, k_scale_tok=None, v_scale_tok=None):
     qa, qk = _raw(q, q_dtype)
     ka, kk = _raw(k_cache, kv_dtype)
     va, vk = _raw(v_cache, kv_dtype)
@@ -148,30 +175,39 @@ def _problem(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *, scal
         raise ValueError("shape mismatch")
     if qb is not None and qq_bias_stride is None:
         qq_bias_stride = qb.shape[-1]
-    keep = [qa, ka, va, cu, sl, bt, al, qb, sk]
+    kt, ktp, kts = _tok_scale(k_scale_tok)
+    vt, vtp, vts = _tok_scale(v_scale_tok)
+    for t in (kt, vt):
+        if t is not None and (t.shape[0] != num_blocks or t.shape[1] != block_size or
+                              t.shape[2] != hkv):
+            raise ValueError("per-token scales are [num_blocks, block_size, H_kv]")
+    keep = [qa, ka, va, cu, sl, bt, al, qb, sk, kt, vt]
     ptr = lambda a: None if a is None else a.ctypes.data  # noqa: E731
     prob = Problem(ptr(qa), ptr(ka), ptr(va), ptr(cu), ptr(sl), ptr(bt), ptr(al), ptr(qb), ptr(sk),
                    qk, kk, len(sl), bt.shape[1], num_blocks, block_size, hq, hkv, d,
                    -1 if window_left is None else int(window_left),
                    int(qq_bias_stride or 0), float(scale), float(softcap or 0.0),
-                   float(k_scale), float(v_scale))
+                   float(k_scale), float(v_scale), ktp, vtp,
+                   (ctypes.c_int64 * 3)(*kts), (ctypes.c_int64 * 3)(*vts))
     return prob, keep, total_q, hq, d
 
 
 def attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *, scale, softcap=0.0,
               window_left=-1, alibi_slopes=None, qq_bias=None, qq_bias_stride=None, sinks=None,
               k_scale=1.0, v_scale=1.0, q_dtype=None, kv_dtype=None, n_part=0, threads=1,
-              token_range=None, head_range=None):
+              token_range=None, head_range=None, k_scale_tok=None, v_scale_tok=None):
     """Attention output [total_q, H_q, D] in float64.
 
     ``n_part <= 0`` evaluates the plain definition; ``n_part >= 1`` evaluates the
     split-KV partition/merge form.  Rows outside ``token_range``/``head_range`` stay 0.
+    ``k_scale_tok`` / ``v_scale_tok``: fp8 per-token scales [num_blocks, block_size, H_kv]
+    (any strides) in place of the per-tensor ``k_scale`` / ``v_scale``.
     """
     prob, keep, total_q, hq, d = _problem(
         q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, scale=scale, softcap=softcap,
         window_left=window_left, alibi_slopes=alibi_slopes, qq_bias=qq_bias,
         qq_bias_stride=qq_bias_stride, sinks=sinks, k_scale=k_scale, v_scale=v_scale,
-        q_dtype=q_dtype, kv_dtype=kv_dtype)
+        q_dtype=q_dtype, kv_dtype=kv_dtype, k_scale_tok=k_scale_tok, v_scale_tok=v_scale_tok)
     out = np.zeros((total_q, hq, d), dtype=np.float64)
     t0, t1 = token_range or (0, total_q)
     h0, h1 = head_range or (0, hq)
@@ -197,13 +233,13 @@ def attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *, sca
 def attention_rows(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, tokens, heads, *,
                    scale, softcap=0.0, window_left=-1, alibi_slopes=None, qq_bias=None,
                    qq_bias_stride=None, sinks=None, k_scale=1.0, v_scale=1.0, q_dtype=None,
-                   kv_dtype=None, threads=1):
+                   kv_dtype=None, threads=1, k_scale_tok=None, v_scale_tok=None):
     """Selected output rows: result[r] is the row of (tokens[r], heads[r]), float64 [n, D]."""
     prob, keep, total_q, hq, d = _problem(
         q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, scale=scale, softcap=softcap,
         window_left=window_left, alibi_slopes=alibi_slopes, qq_bias=qq_bias,
         qq_bias_stride=qq_bias_stride, sinks=sinks, k_scale=k_scale, v_scale=v_scale,
-        q_dtype=q_dtype, kv_dtype=kv_dtype)
+        q_dtype=q_dtype, kv_dtype=kv_dtype, k_scale_tok=k_scale_tok, v_scale_tok=v_scale_tok)
     tok = np.ascontiguousarray(tokens, dtype=np.int32)
     hd = np.ascontiguousarray(heads, dtype=np.int32)
     out = np.zeros((len(tok), d), dtype=np.float64)

@@ -30,6 +30,11 @@
  *     m    = max(sink_h (if sinks), max_j s_j)
  *     den  = exp(sink_h - m) (if sinks) + sum_j exp(s_j - m)
  *     o    = sum_j exp(s_j - m) V_j / den             (fp8: V_j = e4m3(v) * v_scale)
+ *   fp8 scales are per tensor (k_scale, v_scale) or, after the same aiter PR's test
+ *   matrix ("scalar and per-token scales, K and V scales with different strides"), per
+ *   cached token: the scale of key j's K (V) row of kv-head g is the element (block,
+ *   slot, g) of its own array, block = block_table[b][j / block_size] and
+ *   slot = j % block_size, at block * stride0 + slot * stride1 + g * stride2.
  *   A row with no allowed key is 0, with or without a sink (rows of a sequence
  *   with kv_len < q_len whose position p is negative have no key).
  *
@@ -73,6 +78,12 @@ typedef struct {
   int32_t qq_bias_stride;
   double scale, softcap; /* softcap <= 0: off */
   double k_scale, v_scale;
+  /* fp8 per-token scales (NULL: the per-tensor k_scale / v_scale); element strides of
+     block, slot and kv-head */
+  const float* k_scale_tok;
+  const float* v_scale_tok;
+  int64_t k_scale_strides[3];
+  int64_t v_scale_strides[3];
 } ua_ref_problem;
 
 double ua_ref_decode_f16(uint16_t h) {
@@ -126,6 +137,17 @@ static int cache_row(const ua_ref_problem* P, int b, int j, int g, size_t* row) 
   return REF_OK;
 }
 
+/* The fp8 scale of key j's K (which = 0) or V (which = 1) row of kv-head g; 1 for 16-bit
+   caches. */
+static double kv_scale_of(const ua_ref_problem* P, int which, int b, int j, int g) {
+  if (P->kv_dtype != REF_E4M3) return 1.0;
+  const float* tok = which ? P->v_scale_tok : P->k_scale_tok;
+  if (!tok) return which ? P->v_scale : P->k_scale;
+  const int64_t* st = which ? P->v_scale_strides : P->k_scale_strides;
+  int64_t blk = P->block_table[(size_t)b * P->max_blocks_per_seq + j / P->block_size];
+  return (double)tok[blk * st[0] + (int64_t)(j % P->block_size) * st[1] + (int64_t)g * st[2]];
+}
+
 /*
  * Allowed key range [*lo, *hi) of query row i of sequence b.  A row whose position
  * p = ctx + i is negative (only when kv_len < q_len, e.g. a decode slot whose
@@ -149,7 +171,7 @@ static int score(const ua_ref_problem* P, int b, int t, int i, int h, int ctx, i
   size_t row;
   int rc = cache_row(P, b, j, h / G, &row);
   if (rc) return rc;
-  double kscale = P->kv_dtype == REF_E4M3 ? P->k_scale : 1.0;
+  double kscale = kv_scale_of(P, 0, b, j, h / G);
   double dot = 0.0;
   for (int d = 0; d < D; ++d) {
     double qd = load_elem(P->q, P->q_dtype, ((size_t)t * P->num_q_heads + h) * D + d);
@@ -169,7 +191,7 @@ static int add_value_row(const ua_ref_problem* P, int b, int j, int g, double w,
   size_t row;
   int rc = cache_row(P, b, j, g, &row);
   if (rc) return rc;
-  double vscale = P->kv_dtype == REF_E4M3 ? P->v_scale : 1.0;
+  double vscale = kv_scale_of(P, 1, b, j, g);
   for (int d = 0; d < D; ++d) acc[d] += w * load_elem(P->v_cache, P->kv_dtype, row * D + d) * vscale;
   return REF_OK;
 }

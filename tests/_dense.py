@@ -13,13 +13,17 @@ import torch
 
 def dense_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *, scale,
                     softcap=0.0, window_left=-1, alibi_slopes=None, qq_bias=None,
-                    qq_bias_stride=None, sinks=None, k_scale=1.0, v_scale=1.0, **_):
+                    qq_bias_stride=None, sinks=None, k_scale=1.0, v_scale=1.0, k_scale_tok=None,
+                    v_scale_tok=None, **_):
     qd = q.to(torch.float64).numpy()
     kd = k_cache.to(torch.float64).numpy()
     vd = v_cache.to(torch.float64).numpy()
     if k_cache.dtype == torch.float8_e4m3fn:
-        kd = kd * k_scale
-        vd = vd * v_scale
+        # per-token scales [num_blocks, block_size, H_kv] broadcast over the head dim
+        kd = kd * (k_scale if k_scale_tok is None else
+                   k_scale_tok.to(torch.float64).numpy()[..., None])
+        vd = vd * (v_scale if v_scale_tok is None else
+                   v_scale_tok.to(torch.float64).numpy()[..., None])
     cu = cu_seqlens_q.numpy()
     sl = seq_lens_k.numpy()
     bt = block_table.numpy()

@@ -89,6 +89,32 @@ def test_oracle_equals_dense_brute_force(feat, dtypes):
     assert np.abs(got - want).max() <= 1e-12
 
 
+@pytest.mark.parametrize("feat", [dict(), dict(window=5, sinks=True), dict(softcap=0.9, alibi=True)])
+@pytest.mark.parametrize("bs", [13, 16])
+def test_oracle_per_token_scales_equal_dense_brute_force(feat, bs):
+    """fp8 with one K and one V scale per cached token (V's scales with other strides)."""
+    spec = small_spec(seed=60 + bs, q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
+                      block_size=bs, per_token_scales=True, **feat)
+    inp = W.make(spec)
+    assert inp.k_scale_tok.stride() != inp.v_scale_tok.stride()
+    got, want = run_both(inp)
+    assert np.abs(got - want).max() <= 1e-12
+
+
+def test_uniform_per_token_scales_equal_the_per_tensor_scale():
+    inp = W.make(small_spec(seed=61, q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
+                            sinks=True, window=9))
+    kw = inp.oracle_kwargs()
+    ks, vs = float(np.float32(inp.k_scale)), float(np.float32(inp.v_scale))  # float32 values
+    kw.update(k_scale=ks, v_scale=vs)
+    base = oracle.attention(**kw)
+    shape = inp.k_cache.shape[:3]
+    kw.update(k_scale_tok=torch.full(shape, ks, dtype=torch.float32),
+              v_scale_tok=torch.full(shape[::-1], vs, dtype=torch.float32).permute(2, 1, 0),
+              k_scale=7.0, v_scale=9.0)  # ignored when per-token scales are given
+    assert np.array_equal(oracle.attention(**kw), base)
+
+
 @pytest.mark.parametrize("bs", [1, 13, 16, 32, 784])
 @pytest.mark.parametrize("heads", [(4, 4), (8, 2), (7, 1), (6, 3)])
 def test_oracle_block_sizes_and_groups(bs, heads):
@@ -180,10 +206,12 @@ def test_rows_sum_to_one():
     assert np.abs(got2 - got2[..., :1]).max() <= 1e-15
 
 
-@pytest.mark.parametrize("kv_dtype", [torch.float16, torch.float8_e4m3fn])
-def test_block_table_permutation_is_bit_exact(kv_dtype):
+@pytest.mark.parametrize("kv_dtype,per_token", [(torch.float16, False),
+                                                (torch.float8_e4m3fn, False),
+                                                (torch.float8_e4m3fn, True)])
+def test_block_table_permutation_is_bit_exact(kv_dtype, per_token):
     inp = W.make(small_spec(seed=7, kv_dtype=kv_dtype, q_dtype=torch.float16, sinks=True,
-                            window=10, num_blocks=24))
+                            window=10, num_blocks=24, per_token_scales=per_token))
     base = oracle.attention(**inp.oracle_kwargs())
     g = torch.Generator().manual_seed(99)
     perm = torch.randperm(inp.k_cache.shape[0], generator=g)   # new position of block b
@@ -194,6 +222,11 @@ def test_block_table_permutation_is_bit_exact(kv_dtype):
     bt2 = perm[inp.block_table.long()].to(torch.int32)
     kw = inp.oracle_kwargs()
     kw.update(k_cache=k2, v_cache=v2, block_table=bt2)
+    if per_token:  # the scales move with their blocks
+        ks2, vs2 = torch.empty_like(inp.k_scale_tok), torch.empty_like(inp.v_scale_tok)
+        ks2[perm] = inp.k_scale_tok
+        vs2[perm] = inp.v_scale_tok
+        kw.update(k_scale_tok=ks2, v_scale_tok=vs2)
     assert np.array_equal(oracle.attention(**kw), base)
 
 

@@ -31,7 +31,12 @@ MUTANTS = {
     "sink_dropped_from_den": ("double den = P->sinks ? exp((double)P->sinks[h] - m) : 0.0;",
                               "double den = 0.0;"),
     "group_interleaved": ("add_value_row(P, b, j, h / G, w, acc)", "add_value_row(P, b, j, h % P->num_kv_heads, w, acc)"),
-    "v_scale_dropped": ("double vscale = P->kv_dtype == REF_E4M3 ? P->v_scale : 1.0;", "double vscale = 1.0;"),
+    "v_scale_dropped": ("double vscale = kv_scale_of(P, 1, b, j, g);", "double vscale = 1.0;"),
+    "k_token_scale_for_v": ("double vscale = kv_scale_of(P, 1, b, j, g);",
+                            "double vscale = kv_scale_of(P, 0, b, j, g);"),
+    "token_scale_slot_stride": ("(int64_t)(j % P->block_size) * st[1]",
+                                "(int64_t)(j % P->block_size) * st[2]"),
+    "token_scale_head_dropped": ("+ (int64_t)g * st[2]", "+ 0 * st[2]"),
     "slot_from_wrong_block": ("(size_t)(j % P->block_size)", "(size_t)((j + 1) % P->block_size)"),
 }
 
@@ -39,6 +44,7 @@ PROBES = [
     dict(alibi=True, window=7, sinks=True),
     dict(qq_bias=True, qq_bias_shape=(8, 64), qq_bias_std=0.5, softcap=0.8),
     dict(kv_dtype=torch.float8_e4m3fn, q_dtype=torch.bfloat16, window=5),
+    dict(kv_dtype=torch.float8_e4m3fn, q_dtype=torch.bfloat16, per_token_scales=True, sinks=True),
 ]
 
 
@@ -75,5 +81,7 @@ def test_pins_reject_mutant(tmp_path, name):
         spec = W.Spec(name="m", seqs=[(1, 37), (5, 18), (7, 7), (3, 40)], num_q_heads=8,
                       num_kv_heads=2, head_dim=16, block_size=16, seed=40 + i, **feat)
         inp = W.make(spec)
-        worst = max(worst, float(np.abs(_run(lib, inp) - dense_attention(**inp.oracle_kwargs())).max()))
+        diff = np.abs(_run(lib, inp) - dense_attention(**inp.oracle_kwargs()))
+        # a mutant that reads out of range can return NaN, which max() would skip
+        worst = max(worst, float("inf") if np.isnan(diff).any() else float(diff.max()))
     assert worst > 1e-6, f"mutant {name} survived the pins"

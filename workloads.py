@@ -51,6 +51,7 @@ class Spec:
     qq_bias_std: float = 0.1
     sinks: bool = False
     scale: Optional[float] = None           # default 1/sqrt(D)
+    per_token_scales: bool = False          # fp8: one K and one V scale per cached token
     desc: str = ""
 
 
@@ -72,6 +73,9 @@ class Inputs:
     sinks: Optional[torch.Tensor]
     k_scale: float = 1.0
     v_scale: float = 1.0
+    # fp8 per-token scales [num_blocks, block_size, H_kv] (float32; V's with other strides)
+    k_scale_tok: Optional[torch.Tensor] = None
+    v_scale_tok: Optional[torch.Tensor] = None
     extra: dict = field(default_factory=dict)
 
     @property
@@ -106,7 +110,8 @@ class Inputs:
                     scale=self.scale, softcap=self.softcap, window_left=self.window_left,
                     alibi_slopes=self.alibi_slopes, qq_bias=self.qq_bias,
                     qq_bias_stride=self.qq_bias_stride if self.qq_bias is not None else None,
-                    sinks=self.sinks, k_scale=self.k_scale, v_scale=self.v_scale)
+                    sinks=self.sinks, k_scale=self.k_scale, v_scale=self.v_scale,
+                    k_scale_tok=self.k_scale_tok, v_scale_tok=self.v_scale_tok)
 
 
 def alibi_slopes(num_heads: int) -> torch.Tensor:
@@ -165,7 +170,22 @@ def make(spec: Spec, *, poison: bool = False, replicas: int = 1) -> Inputs:
                 used[int(bt[s, j]), :n_slots] = True
 
     k_scale = v_scale = 1.0
-    if spec.kv_dtype == torch.float8_e4m3fn:
+    k_tok = v_tok = None
+    if spec.kv_dtype == torch.float8_e4m3fn and spec.per_token_scales:
+        # one scale per (block, slot, kv-head) row: absmax / 448 (1 for an all-zero row);
+        # V's scales live in a [H_kv, blocks, slots] buffer viewed as [blocks, slots, H_kv]
+        # so that K and V scales have different strides
+        def row_scale(x):
+            s = x.abs().amax(dim=-1) / F8_MAX
+            return torch.where(s > 0, s, torch.ones_like(s)).to(torch.float32)
+        k_tok = row_scale(kf).contiguous()
+        v_tok = row_scale(vf).permute(2, 0, 1).contiguous().permute(1, 2, 0)
+        k_cache = (kf / k_tok[..., None]).clamp(-F8_MAX, F8_MAX).to(torch.float8_e4m3fn)
+        v_cache = (vf / v_tok[..., None]).clamp(-F8_MAX, F8_MAX).to(torch.float8_e4m3fn)
+        if poison:  # scales of slots no sequence owns: never read
+            k_tok[~used] = float("nan")
+            v_tok[~used] = float("nan")
+    elif spec.kv_dtype == torch.float8_e4m3fn:
         k_scale = float(kf[used].abs().max()) / F8_MAX if used.any() else 1.0
         v_scale = float(vf[used].abs().max()) / F8_MAX if used.any() else 1.0
         k_cache = (kf / k_scale).clamp(-F8_MAX, F8_MAX).to(torch.float8_e4m3fn)
@@ -199,7 +219,8 @@ def make(spec: Spec, *, poison: bool = False, replicas: int = 1) -> Inputs:
                   window_left=(spec.window - 1) if spec.window else -1,
                   alibi_slopes=alibi, qq_bias=qq,
                   qq_bias_stride=spec.qq_bias_shape[1] if spec.qq_bias else 0,
-                  sinks=sinks, k_scale=k_scale, v_scale=v_scale)
+                  sinks=sinks, k_scale=k_scale, v_scale=v_scale, k_scale_tok=k_tok,
+                  v_scale_tok=v_tok)
 
 
 # --- the five workloads ------------------------------------------------------------
