@@ -198,6 +198,8 @@ class Call:
         if inp.spec.kv_dtype == torch.float8_e4m3fn:
             self.kv_scale = torch.tensor([inp.k_scale, inp.v_scale], dtype=torch.float32,
                                          device=dev)
+        # per-token fp8 scales keep their strides (V's differ from K's)
+        self.tok = [None if t is None else t.to(dev) for t in (inp.k_scale_tok, inp.v_scale_tok)]
         self.out = torch.empty_like(self.d["q"])
         self.backend = ua.BACKENDS[backend]
         self.plan = ua.plan(num_seqs=inp.num_seqs, total_q=inp.total_q,
@@ -211,7 +213,8 @@ class Call:
                             num_blocks=self.d["k_cache"].shape[0])
         self.shape = ua._shape(self.d["q"], self.d["k_cache"], self.tables[0],
                                self.d["cu_seqlens_q"], inp.max_seqlen_q, inp.max_seqlen_k,
-                               self.d["qq_bias"], ua._DTYPES[self.out.dtype], 0, None, None)
+                               self.d["qq_bias"], ua._DTYPES[self.out.dtype], 0, None, None,
+                               self.tok[0], self.tok[1])
         p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
         spec = inp.spec
         self.head = [p(self.d["q"]), p(self.d["k_cache"]), p(self.d["v_cache"]), p(self.out),
@@ -397,7 +400,8 @@ def run_ours(args):
                                  scale=inp.scale, softcap=inp.softcap,
                                  window_left=inp.window_left, alibi_slopes=call.d["alibi_slopes"],
                                  qq_bias=call.d["qq_bias"], sinks=call.d["sinks"],
-                                 kv_scale=call.kv_scale, out=call.out, stream=stream)
+                                 kv_scale=call.kv_scale, k_scale_tok=call.tok[0],
+                                 v_scale_tok=call.tok[1], out=call.out, stream=stream)
             out_host.copy_(call.out, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()

@@ -100,6 +100,20 @@ typedef struct {
   size_t workspace_bytes;     /* bytes at `workspace` */
   void* events;               /* NULL, or cudaEvent_t[3] recorded on `stream` before the
                                  attention kernel, after it, and after the merge kernel */
+  /* fp8 caches: per-token scales (aiter PR #3962 "split-K long-context decode for shuffled
+   * fp8 SWA", test matrix: per-token scales, K and V scales with different strides), or
+   * NULL for the per-tensor kv_scale.  Device float32 arrays over (block, slot, kv-head):
+   * the scale of key slot s of physical block b, kv-head g, is
+   * k_scale_tok[b * k_scale_stride[0] + s * k_scale_stride[1] + g * k_scale_stride[2]]
+   * (strides in elements, each >= 0); V likewise with its own strides.  Both or neither;
+   * ignored for fp16 / bf16 caches.  Read by the decode tile (at most 8 rows per kv-head,
+   * head_dim <= 128, 16 | block_size); other calls with them return UA_ERR_UNSUPPORTED.
+   * Every scale a call reads must be finite, and V scales below 256 (a key's P times its V
+   * scale is an f16 MMA operand). */
+  const float* k_scale_tok;
+  const float* v_scale_tok;
+  int64_t k_scale_stride[3];
+  int64_t v_scale_stride[3];
 } ua_shape_t;
 
 /* What the dispatcher chose for a call (see ua_plan). */

@@ -17,6 +17,10 @@ def to_dev(inp, dev="cuda"):
     d["kv_scale"] = None
     if inp.spec.kv_dtype == torch.float8_e4m3fn:
         d["kv_scale"] = torch.tensor([inp.k_scale, inp.v_scale], dtype=torch.float32, device=dev)
+    # per-token scales keep their strides (V's differ from K's)
+    for name in ("k_scale_tok", "v_scale_tok"):
+        t = getattr(inp, name)
+        d[name] = None if t is None else t.to(dev)
     return d
 
 
@@ -28,7 +32,9 @@ def run(inp, backend="auto", out_dtype=torch.float32, dev_inputs=None, replica=0
                                max_seqlen_k=inp.max_seqlen_k, scale=inp.scale,
                                softcap=inp.softcap, window_left=inp.window_left,
                                alibi_slopes=d["alibi_slopes"], qq_bias=d["qq_bias"],
-                               sinks=d["sinks"], kv_scale=d["kv_scale"], out_dtype=out_dtype,
+                               sinks=d["sinks"], kv_scale=d["kv_scale"],
+                               k_scale_tok=d["k_scale_tok"], v_scale_tok=d["v_scale_tok"],
+                               out_dtype=out_dtype,
                                backend=backend, **kw)
     torch.cuda.synchronize()
     return out

@@ -38,7 +38,7 @@ def inputs(spec):
     return _INPUT_CACHE[spec.name]
 
 
-FULL = [W.TINY, W.DECODE, W.MIXED, W.SWDECODE_BF16, W.SWDECODE_FP8]
+FULL = [W.TINY, W.DECODE, W.MIXED, W.SWDECODE_BF16, W.SWDECODE_FP8, W.SWDECODE_FP8_TOK]
 
 
 @pytest.mark.parametrize("backend", ["auto", "2d", "split"])
@@ -133,6 +133,14 @@ SMALL = {
                                  kv_dtype=torch.bfloat16, window=200, sinks=True),
     "dec_f16_d64_g8": dict(seqs=[(1, 500), (1, 31), (1, 16)], num_q_heads=16, num_kv_heads=2,
                             head_dim=64, block_size=32),
+    # fp8 with per-token K and V scales (V's with other strides), on the decode tile
+    "dec_fp8_tok_feat": dict(seqs=[(1, 700), (2, 129), (1, 1), (1, 17), (1, 0), (4, 333)],
+                             num_q_heads=8, num_kv_heads=4, kv_dtype=torch.float8_e4m3fn,
+                             q_dtype=torch.bfloat16, per_token_scales=True, softcap=25.0,
+                             alibi=True, sinks=True, window=260),
+    "dec_fp8_tok_d64_bs32": dict(seqs=[(1, 900), (1, 65), (1, 31)], num_q_heads=16,
+                                 num_kv_heads=2, head_dim=64, block_size=32,
+                                 kv_dtype=torch.float8_e4m3fn, per_token_scales=True),
     # 9 to 16 rows per kv-head, and head_dim 256: the 16-row tile kernel's decode path
     "tile16_bf16_g8_q2": dict(seqs=[(2, 700), (1, 300), (2, 45), (1, 1)], num_q_heads=16,
                               num_kv_heads=2, q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16,
@@ -162,11 +170,14 @@ def test_forced_partition_counts(n_part):
     assert max_err(out, want) <= 2e-3
 
 
-@pytest.mark.parametrize("kv,decode", [(torch.float16, False), (torch.float8_e4m3fn, False),
-                                       (torch.float8_e4m3fn, True)])
-def test_block_table_permutation_is_bit_exact(kv, decode):
+@pytest.mark.parametrize("kv,decode,tok", [(torch.float16, False, False),
+                                           (torch.float8_e4m3fn, False, False),
+                                           (torch.float8_e4m3fn, True, False),
+                                           (torch.float8_e4m3fn, True, True)])
+def test_block_table_permutation_is_bit_exact(kv, decode, tok):
     extra = dict(seqs=[(1, 300), (1, 45), (2, 100)], num_q_heads=8, num_kv_heads=4) if decode else {}
-    spec = _small(7, kv_dtype=kv, window=100, sinks=True, num_blocks=80, **extra)
+    spec = _small(7, kv_dtype=kv, window=100, sinks=True, num_blocks=80, per_token_scales=tok,
+                  **extra)
     inp = W.make(spec)
     base = run(inp, backend="split").cpu()
     perm = torch.randperm(inp.k_cache.shape[0], generator=torch.Generator().manual_seed(5))
@@ -174,6 +185,11 @@ def test_block_table_permutation_is_bit_exact(kv, decode):
     k2.view(torch.uint8)[perm] = inp.k_cache.view(torch.uint8)
     v2.view(torch.uint8)[perm] = inp.v_cache.view(torch.uint8)
     inp2 = replace(inp, k_cache=k2, v_cache=v2, block_table=perm[inp.block_table.long()].int())
+    if tok:  # the scales move with their blocks
+        ks2, vs2 = torch.empty_like(inp.k_scale_tok), torch.empty_like(inp.v_scale_tok)
+        ks2[perm] = inp.k_scale_tok
+        vs2[perm] = inp.v_scale_tok
+        inp2 = replace(inp2, k_scale_tok=ks2, v_scale_tok=vs2)
     for backend in ("split", "2d"):
         ref = run(inp, backend=backend).cpu()
         got = run(inp2, backend=backend).cpu()
@@ -292,6 +308,18 @@ def test_cuda_graph_capture_and_replay(spec, kw):
         kwargs["q"] = inp.q * qmul
         want = oracle.attention(threads=THREADS, **kwargs)
         assert max_err(out, want) <= TOL[spec.kv_dtype], (spec.name, replica)
+
+
+def test_per_token_scales_outside_the_decode_tile_are_unsupported():
+    # prefill-shaped rows (more than 8 per kv-head): no kernel reads per-token scales
+    inp = W.make(_small(11, kv_dtype=torch.float8_e4m3fn, per_token_scales=True))
+    with pytest.raises(ua.UaError) as e:
+        run(inp)
+    assert e.value.code == ua._lib.UA_ERR_UNSUPPORTED
+    # only one of the two scale arrays
+    inp = W.make(_small(12, seqs=[(1, 100)], kv_dtype=torch.float8_e4m3fn, per_token_scales=True))
+    with pytest.raises(ValueError):
+        run(replace(inp, v_scale_tok=None))
 
 
 def test_out_of_range_block_id_is_reported_not_read():

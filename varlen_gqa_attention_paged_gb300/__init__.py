@@ -47,7 +47,7 @@ def _ptr(t):
 
 
 def _shape(q, k_cache, block_table, cu_seqlens_q, max_seqlen_q, max_seqlen_k, qq_bias,
-           out_dtype_code, num_splits, workspace, events):
+           out_dtype_code, num_splits, workspace, events, k_scale_tok=None, v_scale_tok=None):
     sh = _lib.UaShape()
     sh.num_seqs = cu_seqlens_q.numel() - 1
     sh.total_q = q.shape[0]
@@ -69,13 +69,25 @@ def _shape(q, k_cache, block_table, cu_seqlens_q, max_seqlen_q, max_seqlen_k, qq
         arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
         sh.events = ctypes.cast(arr, ctypes.c_void_p)
         sh._events_keepalive = arr  # noqa: SLF001 -- keep the array alive for the call
+    if (k_scale_tok is None) != (v_scale_tok is None):
+        raise ValueError("per-token scales: give both k_scale_tok and v_scale_tok, or neither")
+    if k_scale_tok is not None:
+        for t, ptr, strides in ((k_scale_tok, "k_scale_tok", "k_scale_stride"),
+                                (v_scale_tok, "v_scale_tok", "v_scale_stride")):
+            if t.dtype != torch.float32 or not t.is_cuda or t.dim() != 3:
+                raise ValueError("per-token scales are float32 CUDA tensors [blocks, slots, H_kv]")
+            if tuple(t.shape) != tuple(k_cache.shape[:3]):
+                raise ValueError("per-token scales must be [num_blocks, block_size, H_kv]")
+            setattr(sh, ptr, t.data_ptr())
+            setattr(sh, strides, (ctypes.c_int64 * 3)(*t.stride()))
     return sh
 
 
 def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *,
                       max_seqlen_q: int, max_seqlen_k: int, scale: float | None = None,
                       softcap: float = 0.0, window_left: int = -1, alibi_slopes=None,
-                      qq_bias=None, sinks=None, kv_scale=None, out=None, out_dtype=None,
+                      qq_bias=None, sinks=None, kv_scale=None, k_scale_tok=None,
+                      v_scale_tok=None, out=None, out_dtype=None,
                       backend: str = "auto", num_splits: int = 0, workspace=None, stream=None,
                       events=None):
     """Paged varlen GQA attention on the GPU; returns ``out`` [total_q, H_q, D].
@@ -83,7 +95,9 @@ def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table
     q [total_q, H_q, D] f16/bf16; k_cache, v_cache [num_blocks, block_size, H_kv, D]
     f16/bf16/float8_e4m3fn; cu_seqlens_q [S+1], seq_lens_k [S], block_table [S, max_blocks]
     int32; alibi_slopes / sinks [H_q] and qq_bias [rows, stride] float32; kv_scale float32[2]
-    (k_scale, v_scale) for the fp8 cache.  max_seqlen_q / max_seqlen_k are host ints.
+    (k_scale, v_scale) for the fp8 cache, or k_scale_tok / v_scale_tok float32 [num_blocks,
+    block_size, H_kv] (any strides) for per-token fp8 scales.  max_seqlen_q / max_seqlen_k
+    are host ints.
     """
     lib = _lib.load()
     total_q, hq, d = q.shape
@@ -105,7 +119,7 @@ def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     sh = _shape(q, k_cache, block_table, cu_seqlens_q, max_seqlen_q, max_seqlen_k, qq_bias,
-                _dtype_code(out), num_splits, workspace, events)
+                _dtype_code(out), num_splits, workspace, events, k_scale_tok, v_scale_tok)
     rc = lib.ua_unified_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(cu_seqlens_q), _ptr(seq_lens_k),
         _ptr(block_table), block_size, hq, hkv, d, float(scale), float(softcap or 0.0),

@@ -38,6 +38,10 @@ class UaShape(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("events", ctypes.c_void_p),
+        ("k_scale_tok", ctypes.c_void_p),
+        ("v_scale_tok", ctypes.c_void_p),
+        ("k_scale_stride", ctypes.c_int64 * 3),
+        ("v_scale_stride", ctypes.c_int64 * 3),
     ]
 
 

@@ -294,7 +294,18 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
     return UA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return UA_ERR_INVALID_ARG;
-  if (kv_dtype == UA_DT_F8E4M3 && kv_scale == nullptr) return UA_ERR_INVALID_ARG;
+  const bool tok_scales = kv_dtype == UA_DT_F8E4M3 && sh->k_scale_tok != nullptr;
+  if (kv_dtype == UA_DT_F8E4M3) {
+    if ((sh->k_scale_tok == nullptr) != (sh->v_scale_tok == nullptr)) return UA_ERR_INVALID_ARG;
+    if (!tok_scales && kv_scale == nullptr) return UA_ERR_INVALID_ARG;
+    if (tok_scales) {
+      if ((reinterpret_cast<uintptr_t>(sh->k_scale_tok) & 3) ||
+          (reinterpret_cast<uintptr_t>(sh->v_scale_tok) & 3))
+        return UA_ERR_INVALID_ARG;
+      for (int i = 0; i < 3; ++i)
+        if (sh->k_scale_stride[i] < 0 || sh->v_scale_stride[i] < 0) return UA_ERR_INVALID_ARG;
+    }
+  }
   if (qq_bias != nullptr && sh->qq_bias_stride < std::max(1, sh->max_seqlen_q))
     return UA_ERR_INVALID_ARG;
   if (sh->max_blocks_per_seq < 1 || sh->num_blocks < 1) return UA_ERR_INVALID_ARG;
@@ -319,6 +330,14 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   p.qq_bias = qq_bias;
   p.sinks = sinks;
   p.kv_scale = kv_scale;
+  if (tok_scales) {
+    p.k_scale_tok = sh->k_scale_tok;
+    p.v_scale_tok = sh->v_scale_tok;
+    for (int i = 0; i < 3; ++i) {
+      p.k_scale_stride[i] = sh->k_scale_stride[i];
+      p.v_scale_stride[i] = sh->v_scale_stride[i];
+    }
+  }
   p.num_seqs = sh->num_seqs;
   p.total_q = sh->total_q;
   p.max_seqlen_q = sh->max_seqlen_q;
@@ -370,6 +389,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
               true, &pl);
     p.n_part = pl.n_part;
   }
+  // per-token fp8 scales: the decode tile reads them (decode batches, head_dim <= 128,
+  // 16 | block_size); other shapes have no kernel for them
+  if (tok_scales && pl.kernel != ua::KERNEL_DEC8) return UA_ERR_UNSUPPORTED;
   p.cluster_merge = pl.cluster_z > 1 ? 1 : 0;
   if (pl.n_part > 1 && !p.cluster_merge) {
     void* ws = sh->workspace;

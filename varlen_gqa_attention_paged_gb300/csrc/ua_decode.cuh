@@ -51,7 +51,9 @@ struct DecCfg {
                                       ? kStages * kStageBytes
                                       : kMergeBytes + kPartBytes;
   static constexpr int kPipeBytes = (kPipeRaw + 1023) & ~1023;
-  static constexpr int kSmemBytes = 1024 + kPipeBytes + 2 * kStages * 8;
+  // fp8 per-token scales of a stage's keys, K then V, behind the barriers
+  static constexpr int kScaleBytes = kPermD ? kStages * 2 * kT * 4 : 0;
+  static constexpr int kSmemBytes = 1024 + kPipeBytes + 2 * kStages * 8 + kScaleBytes;
   static constexpr int kMinBlocks = (3 * (kSmemBytes + 1024) <= 228 * 1024) ? 3 : 2;
   static_assert(D <= 128, "the key-major decode tile covers head_dim <= 128");
   static_assert(kRowBytes % kCBW == 0 && kCBW % 16 == 0, "rows are whole column blocks");
@@ -88,6 +90,8 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
   uint8_t* const pipe = smem;
   uint64_t* const full = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
   uint64_t* const empty = full + S;
+  float* const sks = reinterpret_cast<float*>(empty + S);  // [S][T] K scales (per-token fp8)
+  float* const svs = sks + S * T;                           // [S][T] V scales
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
@@ -118,6 +122,9 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
   const int ke = min(ks + part, hi);
   const int ntiles = (ke - ks + T - 1) / T;
   const bool cmerge = p.cluster_merge != 0;
+  // fp8 per-token scales (aiter PR #3962 test matrix): key j's K and V rows carry their own
+  // scale, element (block, slot, g) of two separately strided arrays
+  const bool tok = KV == KV_E4M3 && p.k_scale_tok != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -149,16 +156,49 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
       }
       return blk * bs + key % bs;
     };
+    // per-token scales of this lane's keys 2 lane, 2 lane + 1 of tile t (0 past the walk)
+    auto load_scales = [&](int t, float (&kv)[2][2]) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        kv[e][0] = kv[e][1] = 0.f;
+        const int key = ks + t * T + 2 * lane + e;
+        if (key >= ke) continue;
+        const int col = key / bs;
+        const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) continue;
+        const long long slot = key % bs;
+        kv[e][0] = __ldg(p.k_scale_tok + blk * p.k_scale_stride[0] + slot * p.k_scale_stride[1] +
+                         g * p.k_scale_stride[2]);
+        kv[e][1] = __ldg(p.v_scale_tok + blk * p.v_scale_stride[0] + slot * p.v_scale_stride[1] +
+                         g * p.v_scale_stride[2]);
+      }
+    };
+    float sc_next[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    if (tok && ntiles > 0) load_scales(0, sc_next);
     int issued = 0;
     int row_next = ntiles > 0 ? page_row(0) : oob;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % S;
       const int row = row_next;
       if (t + 1 < ntiles) row_next = page_row(t + 1);  // block-table lookups one tile ahead
+      float sc_cur[2][2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        sc_cur[e][0] = sc_next[e][0];
+        sc_cur[e][1] = sc_next[e][1];
+      }
+      if (tok && t + 1 < ntiles) load_scales(t + 1, sc_next);  // scales one tile ahead
       if (t >= S && !mbar_wait_bounded(&empty[s], ((t / S) & 1) ^ 1, p.status, DEV_TIMEOUT))
         break;
       uint8_t* kdst = pipe + s * C::kStageBytes;
       uint8_t* vdst = kdst + C::kCB * C::kCBBytes;
+      if (tok) {  // visible to the consumers through the stage's barrier (release by lane 0)
+        sks[s * T + 2 * lane] = sc_cur[0][0];
+        sks[s * T + 2 * lane + 1] = sc_cur[1][0];
+        svs[s * T + 2 * lane] = sc_cur[0][1];
+        svs[s * T + 2 * lane + 1] = sc_cur[1][1];
+        __syncwarp();
+      }
       if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
       __syncwarp();
       if (lane < T / 16) {
@@ -186,10 +226,12 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
   // ========================================================== consumer warps
   const int gq = lane >> 2, cq = lane & 3;
 
-  float k_scale = 1.f, v_scale = 1.f;
+  float k_scale = 1.f, v_scale = 1.f;  // per tensor (per-token scales: 1, applied per key)
   if constexpr (KV == KV_E4M3) {
-    k_scale = __ldg(p.kv_scale);
-    v_scale = __ldg(p.kv_scale + 1);
+    if (!tok) {
+      k_scale = __ldg(p.kv_scale);
+      v_scale = __ldg(p.kv_scale + 1);
+    }
   }
   const float scale = p.scale * k_scale;
   const float scale_log2 = scale * kLog2e;
@@ -318,6 +360,16 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
         }
       }
 
+      if constexpr (KV == KV_E4M3) {
+        if (tok) {  // keys gq and gq + 8: their own K scales
+          const float s0 = sks[s * T + 16 * ch + gq], s8 = sks[s * T + 16 * ch + gq + 8];
+          st[0] *= s0;
+          st[1] *= s0;
+          st[2] *= s8;
+          st[3] *= s8;
+        }
+      }
+
       // ---- score transform and mask (log2 domain)
       const bool need_mask = kc0 < lomax || kc0 + 15 > pmin || kc0 + 16 > ke;
 #pragma unroll
@@ -379,6 +431,15 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
       // 2cq + 8, 2cq + 9 (register 1) of row gq.
       uint32_t pb[2], pbl[2];
       if constexpr (kF16Mma) {
+        if constexpr (KV == KV_E4M3) {
+          if (tok) {  // P of keys gq and gq + 8 times their V scales (the row sum took P)
+            const float s0 = svs[s * T + 16 * ch + gq], s8 = svs[s * T + 16 * ch + gq + 8];
+            st[0] *= s0;
+            st[1] *= s0;
+            st[2] *= s8;
+            st[3] *= s8;
+          }
+        }
         pb[0] = movmatrix_trans(pack_f16(st[0], st[1]));
         pb[1] = movmatrix_trans(pack_f16(st[2], st[3]));
       } else {

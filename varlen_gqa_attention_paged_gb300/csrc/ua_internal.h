@@ -27,6 +27,12 @@ struct AttnParams {
   const float* qq_bias;         // [*, qq_stride] or null
   const float* sinks;           // [hq] or null
   const float* kv_scale;        // {k_scale, v_scale} (fp8 cache) or null
+  // fp8 per-token scales over (block, slot, kv-head) with element strides, or null (the
+  // decode tile kernel reads them; kv_scale is then unused)
+  const float* k_scale_tok;
+  const float* v_scale_tok;
+  long long k_scale_stride[3];
+  long long v_scale_stride[3];
   float* ws_m;                  // [total_q, hq, n_part]     (n_part > 1)
   float* ws_l;                  // [total_q, hq, n_part]
   float* ws_acc;                // [total_q, hq, n_part, D]

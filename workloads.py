@@ -237,6 +237,9 @@ SWDECODE_BF16 = Spec("swdecode_bf16", [(1, 6700)] * 8, 32, 8, 128, q_dtype=torch
                      desc="batch 8 decode, kv 6700, window 4096, sinks; 32q/8kv; bf16 KV")
 SWDECODE_FP8 = replace(SWDECODE_BF16, name="swdecode_fp8", kv_dtype=torch.float8_e4m3fn,
                        desc="batch 8 decode, kv 6700, window 4096, sinks; 32q/8kv; fp8 e4m3 KV")
+SWDECODE_FP8_TOK = replace(SWDECODE_FP8, name="swdecode_fp8_tok", per_token_scales=True,
+                           desc="batch 8 decode, kv 6700, window 4096, sinks; 32q/8kv; fp8 e4m3 "
+                                "KV with per-token K and V scales")
 PREFILL_D128 = Spec("prefill_d128", [(4096, 4096)] * 4 + [(2048, 18432)], 32, 8, 128,
                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=4,
                     desc="4x4096 prompts + 2048 chunk behind 16384 prefix; 32q/8kv d128; bf16")
@@ -244,12 +247,13 @@ PREFILL_D256 = replace(PREFILL_D128, name="prefill_d256", num_q_heads=24, num_kv
                        head_dim=256,
                        desc="4x4096 prompts + 2048 chunk behind 16384 prefix; 24q/4kv d256; bf16")
 
-WORKLOADS = {s.name: s for s in (TINY, DECODE, MIXED, SWDECODE_BF16, SWDECODE_FP8, PREFILL_D128,
-                                 PREFILL_D256)}
+WORKLOADS = {s.name: s for s in (TINY, DECODE, MIXED, SWDECODE_BF16, SWDECODE_FP8,
+                                 SWDECODE_FP8_TOK, PREFILL_D128, PREFILL_D256)}
 
 
 def kv_bytes_read(inp: Inputs) -> int:
-    """Algorithmic K+V bytes: every attended key's K and V row read once per kv-head."""
+    """Algorithmic K+V bytes: every attended key's K and V row read once per kv-head (with
+    per-token fp8 scales, also its two 4-byte scales)."""
     spec = inp.spec
     esz = torch.empty((), dtype=spec.kv_dtype).element_size()
     total = 0
@@ -257,7 +261,8 @@ def kv_bytes_read(inp: Inputs) -> int:
         ctx = kv - a
         lo_first = 0 if inp.window_left < 0 else max(0, ctx - inp.window_left)
         total += (kv - lo_first)  # keys touched by at least one row of the sequence
-    return total * spec.num_kv_heads * spec.head_dim * esz * 2
+    per_key = spec.head_dim * esz + (4 if spec.per_token_scales else 0)
+    return total * spec.num_kv_heads * per_key * 2
 
 
 def causal_pairs(inp: Inputs) -> int:
