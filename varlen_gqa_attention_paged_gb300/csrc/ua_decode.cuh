@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      // per-token scales: a second arrival once the stage's scales are in shared memory
+      mbar_init(&full[s], tok ? 2 : 1);
       mbar_init(&empty[s], C::kConsumerWarps);
     }
     s_abort = 0;
@@ -156,16 +157,21 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
       }
       return blk * bs + key % bs;
     };
-    // per-token scales of this lane's keys 2 lane, 2 lane + 1 of tile t (0 past the walk)
-    auto load_scales = [&](int t, float (&kv)[2][2]) {
+    // Per-token scales of this lane's keys 2 lane and 2 lane + 1 of tile t (one page; 0 past
+    // the walk): the page's block id is loaded two tiles ahead, the scales one tile ahead.
+    auto scale_blk = [&](int t) -> int {
+      const int key = ks + t * T + 2 * lane;
+      if (t >= ntiles || key >= ke) return -1;
+      const int col = key / bs;
+      const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+      return static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks) ? blk : -1;
+    };
+    auto load_scales = [&](int t, int blk, float (&kv)[2][2]) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         kv[e][0] = kv[e][1] = 0.f;
         const int key = ks + t * T + 2 * lane + e;
-        if (key >= ke) continue;
-        const int col = key / bs;
-        const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
-        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) continue;
+        if (blk < 0 || key >= ke) continue;
         const long long slot = key % bs;
         kv[e][0] = __ldg(p.k_scale_tok + blk * p.k_scale_stride[0] + slot * p.k_scale_stride[1] +
                          g * p.k_scale_stride[2]);
@@ -174,7 +180,11 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
       }
     };
     float sc_next[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    if (tok && ntiles > 0) load_scales(0, sc_next);
+    int blk_next = -1;
+    if (tok) {
+      if (ntiles > 0) load_scales(0, scale_blk(0), sc_next);
+      blk_next = scale_blk(1);
+    }
     int issued = 0;
     int row_next = ntiles > 0 ? page_row(0) : oob;
     for (int t = 0; t < ntiles; ++t) {
@@ -187,18 +197,14 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
         sc_cur[e][0] = sc_next[e][0];
         sc_cur[e][1] = sc_next[e][1];
       }
-      if (tok && t + 1 < ntiles) load_scales(t + 1, sc_next);  // scales one tile ahead
+      if (tok) {  // scales one tile ahead, block ids two tiles ahead
+        if (t + 1 < ntiles) load_scales(t + 1, blk_next, sc_next);
+        blk_next = scale_blk(t + 2);
+      }
       if (t >= S && !mbar_wait_bounded(&empty[s], ((t / S) & 1) ^ 1, p.status, DEV_TIMEOUT))
         break;
       uint8_t* kdst = pipe + s * C::kStageBytes;
       uint8_t* vdst = kdst + C::kCB * C::kCBBytes;
-      if (tok) {  // visible to the consumers through the stage's barrier (release by lane 0)
-        sks[s * T + 2 * lane] = sc_cur[0][0];
-        sks[s * T + 2 * lane + 1] = sc_cur[1][0];
-        svs[s * T + 2 * lane] = sc_cur[0][1];
-        svs[s * T + 2 * lane + 1] = sc_cur[1][1];
-        __syncwarp();
-      }
       if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
       __syncwarp();
       if (lane < T / 16) {
@@ -210,6 +216,14 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
           tma_load_3d(vdst + cb * C::kCBBytes + lane * 16 * C::kCBW, &tp.tmap_v, x, g, row,
                       &full[s], policy);
         }
+      }
+      if (tok) {  // after the copies are on their way; released to the consumers by lane 0
+        sks[s * T + 2 * lane] = sc_cur[0][0];
+        sks[s * T + 2 * lane + 1] = sc_cur[1][0];
+        svs[s * T + 2 * lane] = sc_cur[0][1];
+        svs[s * T + 2 * lane + 1] = sc_cur[1][1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
       }
       issued = t + 1;
     }
