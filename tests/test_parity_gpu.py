@@ -116,6 +116,18 @@ SMALL = {
                                   qq_bias=True, qq_bias_shape=(64, 64), sinks=True),
     "pf_f16_g6_chunk": dict(seqs=[(70, 600), (1, 17)], num_q_heads=12, num_kv_heads=2,
                             window=300),
+    # fp8 caches on the tensor-memory kernel (head_dim 128): codes dequantised to f16 tiles
+    # in shared memory, a bf16 q converted to f16; one and two q tiles a CTA
+    "pf_fp8_bf16q_window_sinks": dict(seqs=[(200, 500), (129, 129), (1, 300), (37, 45)],
+                                      num_q_heads=32, num_kv_heads=8, q_dtype=torch.bfloat16,
+                                      kv_dtype=torch.float8_e4m3fn, window=150, sinks=True),
+    "pf_fp8_f16q_g16_feat": dict(seqs=[(150, 600), (9, 9)], num_q_heads=16, num_kv_heads=1,
+                                 kv_dtype=torch.float8_e4m3fn, softcap=30.0, alibi=True,
+                                 qq_bias=True, qq_bias_shape=(160, 160), sinks=True),
+    "pf_fp8_bf16q_two_tiles": dict(seqs=[(1500, 1500), (1000, 1600), (300, 300)],
+                                   num_q_heads=32, num_kv_heads=8, block_size=32,
+                                   q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
+                                   window=256),
     # head_dim 256: K and V stream as half tiles through one ring; odd and even tile counts
     "pf_f16_d256_ragged": dict(seqs=[(130, 390), (1, 129), (64, 64), (257, 900)],
                                num_q_heads=8, num_kv_heads=2, head_dim=256),

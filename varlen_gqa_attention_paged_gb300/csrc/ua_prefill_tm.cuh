@@ -28,6 +28,12 @@
 // producers (Q once and K pages; V pages; pages of 16 keys found through the block table,
 // each operand in its own ring, 128-byte swizzled), warp 4NQ+2 MMA issuer and
 // tensor-memory owner.
+//
+// fp8-e4m3 caches (F8, head_dim 128): the producers copy fp8 K and V tiles into a staging
+// buffer, and four more warps (thread = row) turn each into the f16 tile the MMA reads
+// (every e4m3 value is an f16; V rows past kv_len become zeros), after converting a bf16
+// Q to f16 in place once; the MMAs and the softmax then run the f16 path, with k_scale
+// in the score scale and v_scale on the output.
 #pragma once
 
 #include <atomic>
@@ -44,7 +50,7 @@
 
 namespace ua {
 
-template <int D, int NQ>
+template <int D, int NQ, bool F8 = false>
 struct PrefillTmCfg {
   static constexpr int kBM = 128;                        // MMA rows of one q tile
   static constexpr int kBN = 128;                        // keys per tile
@@ -53,30 +59,37 @@ struct PrefillTmCfg {
   static constexpr int kKVCB = kBN * 128;                // one column block of a K or V tile
   static constexpr int kTileBytes = kCB * kKVCB;         // one K (or V) tile
   static constexpr int kBarBytes = 512;
+  // fp8 caches: one staging tile of fp8 codes per operand (128 keys x 128 bytes)
+  static constexpr int kF8Tile = kBN * 128;
+  static constexpr int kF8Bytes = F8 ? 2 * kF8Tile : 0;
+  static constexpr int kDeqWarps = F8 ? 4 : 0;
   // K and V ring depths: as many tiles as fit beside Q (K gets the odd one, at most 4 each)
-  static constexpr int kSlots = (227 * 1024 - 1024 - kBarBytes - NQ * kQBytes) / kTileBytes;
+  static constexpr int kSlots =
+      (227 * 1024 - 1024 - kBarBytes - NQ * kQBytes - kF8Bytes) / kTileBytes;
   static constexpr int kRingK = (kSlots + 1) / 2 > 4 ? 4 : (kSlots + 1) / 2;
   static constexpr int kRingV = kSlots / 2 > 4 ? 4 : kSlots / 2;
   static constexpr int kSmemBytes =
-      1024 + NQ * kQBytes + (kRingK + kRingV) * kTileBytes + kBarBytes;
+      1024 + NQ * kQBytes + (kRingK + kRingV) * kTileBytes + kF8Bytes + kBarBytes;
   static constexpr int kTmemStride = kBN + D;            // S/P, then O, of one q tile
   static constexpr int kTmemCols = 512;
   static constexpr int kSoftmaxWarps = 4 * NQ;
-  static constexpr int kThreads = 32 * kSoftmaxWarps + 96;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 96 + 32 * kDeqWarps;
   static_assert(D <= 128, "two 128-key K/V rings must fit");
   static_assert(NQ * kTmemStride <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kRingK >= 2 && kRingV >= 2, "at least double-buffered K and V");
+  static_assert(!F8 || D == 128, "fp8 caches: head_dim 128 (one 128-byte column block of codes)");
 };
 
-template <int D, int NQ, bool BF16, bool FEAT>
-__global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
+template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
+__global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
     ua_prefill_tm_kernel(const __grid_constant__ PrefillParams pp) {
-  using C = PrefillTmCfg<D, NQ>;
+  using C = PrefillTmCfg<D, NQ, F8>;
   constexpr int BN = C::kBN;
   constexpr int RK = C::kRingK, RV = C::kRingV;
   constexpr int kProducerK = C::kSoftmaxWarps, kProducerV = C::kSoftmaxWarps + 1;
   constexpr int kMma = C::kSoftmaxWarps + 2;
+  constexpr int kDeq0 = C::kSoftmaxWarps + 3;  // fp8: dequant warps kDeq0 .. kDeq0 + 3
   const AttnParams& p = pp.p;
   grid_dependency_wait();
   grid_launch_dependents();
@@ -87,14 +100,22 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
   uint8_t* const sQ = smem;                          // NQ q tiles
   uint8_t* const sK = sQ + NQ * C::kQBytes;          // RK K tiles
   uint8_t* const sV = sK + RK * C::kTileBytes;       // RV V tiles
-  uint64_t* const bars = reinterpret_cast<uint64_t*>(sV + RV * C::kTileBytes);
+  uint8_t* const sK8 = sV + RV * C::kTileBytes;      // fp8: staging K tile of codes
+  uint8_t* const sV8 = sK8 + (F8 ? C::kF8Tile : 0);  // fp8: staging V tile of codes
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(sK8 + C::kF8Bytes);
   uint64_t* const q_full = bars + 0;
   uint64_t* const fin = bars + 1;
   uint64_t* const k_full = bars + 2;                 // [RK]
   uint64_t* const k_empty = k_full + RK;             // [RK]
   uint64_t* const v_full = k_empty + RK;             // [RV]
   uint64_t* const v_empty = v_full + RV;             // [RV]
-  uint64_t* const tile_bars = v_empty + RV;          // [NQ][3]: s_full, p_full, pv_done
+  // fp8: Q converted, staging K / V full (copies) and empty (dequant warps)
+  uint64_t* const q_ready = v_empty + RV;
+  uint64_t* const k8_full = q_ready + 1;
+  uint64_t* const k8_empty = q_ready + 2;
+  uint64_t* const v8_full = q_ready + 3;
+  uint64_t* const v8_empty = q_ready + 4;
+  uint64_t* const tile_bars = v_empty + RV + (F8 ? 5 : 0);  // [NQ][3]: s_full, p_full, pv_done
   auto s_full = [&](int qt) { return tile_bars + 3 * qt; };
   auto p_full = [&](int qt) { return tile_bars + 3 * qt + 1; };
   auto pv_done = [&](int qt) { return tile_bars + 3 * qt + 2; };
@@ -146,13 +167,21 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
+    // f16 tiles are made by the copies, or (fp8) by the dequant warps
     for (int i = 0; i < RK; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], F8 ? C::kDeqWarps : 1);
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < RV; ++i) {
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], F8 ? C::kDeqWarps : 1);
       mbar_init(&v_empty[i], 1);
+    }
+    if constexpr (F8) {
+      mbar_init(q_ready, C::kDeqWarps);
+      mbar_init(k8_full, 1);
+      mbar_init(k8_empty, C::kDeqWarps);
+      mbar_init(v8_full, 1);
+      mbar_init(v8_empty, C::kDeqWarps);
     }
     for (int qt = 0; qt < NQ; ++qt) {
       mbar_init(s_full(qt), 1);
@@ -189,10 +218,13 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     // a V slot.  Block ids are loaded two tiles ahead and only checked when used, so the
     // loop never stalls on a block-table load.
     const bool is_k = warp == kProducerK;
-    const int R = is_k ? RK : RV;
-    uint64_t* const full = is_k ? k_full : v_full;
-    uint64_t* const empty = is_k ? k_empty : v_empty;
-    uint8_t* const ring = is_k ? sK : sV;
+    // fp8: one staging tile of codes per operand instead of the f16 ring
+    const int R = F8 ? 1 : (is_k ? RK : RV);
+    uint64_t* const full = F8 ? (is_k ? k8_full : v8_full) : (is_k ? k_full : v_full);
+    uint64_t* const empty = F8 ? (is_k ? k8_empty : v8_empty) : (is_k ? k_empty : v_empty);
+    uint8_t* const ring = F8 ? (is_k ? sK8 : sV8) : (is_k ? sK : sV);
+    constexpr int kTileIn = F8 ? C::kF8Tile : C::kTileBytes;  // bytes of one copied tile
+    constexpr int kCBIn = F8 ? 1 : C::kCB;                     // its 128-byte column blocks
     const CUtensorMap* const map = is_k ? &pp.tmap_k : &pp.tmap_v;
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
     const int bs = p.block_size;
@@ -228,12 +260,12 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
       blk1 = page_blk(j + 2);
       const int sl = j % R;
       if (j >= R && !pf_wait_warp(&empty[sl], ((j / R) - 1) & 1, abort_flag, p.status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&full[sl], C::kTileBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[sl], kTileIn);
       __syncwarp();
       if (lane < BN / 16)
 #pragma unroll
-        for (int cb = 0; cb < C::kCB; ++cb)
-          tma_load_3d_pf(ring + sl * C::kTileBytes + cb * C::kKVCB + lane * 2048, map, 64 * cb, g,
+        for (int cb = 0; cb < kCBIn; ++cb)
+          tma_load_3d_pf(ring + sl * kTileIn + cb * C::kKVCB + lane * 2048, map, 64 * cb, g,
                          row, &full[sl]);
       issued = j + 1;
     }
@@ -243,6 +275,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     if (is_k && lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
   } else if (warp == kMma) {
     // ======================================================== MMA issuer
+    static_assert(!F8 || !BF16, "fp8 caches run the f16 MMAs");
     // Step j: for each q tile, O += P V_{j-1} (which frees the tile's S/P columns), then
     // S = Q K_j^T.  Tensor-core operations of one thread run in issue order.  The whole
     // warp runs this loop converged; one elected lane issues each MMA and commit.
@@ -251,16 +284,17 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     int jb[NQ], je[NQ];
 #pragma unroll
     for (int qt = 0; qt < NQ; ++qt) tile_walk(qt, jb[qt], je[qt]);
-    bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
+    bool ok = pf_wait_warp(F8 ? q_ready : q_full, 0, abort_flag, p.status);
     for (int j = 0; ok && j <= nt; ++j) {
       const int i = j - 1;  // key tile of this step's P.V
       uint8_t* vs = sV + (i >= 0 ? i % RV : 0) * C::kTileBytes;
       if (i >= 0) {
         if (!pf_wait_warp(&v_full[i % RV], (i / RV) & 1, abort_flag, p.status)) { ok = false; break; }
         // Cache slots at or past kv_len hold no key and may hold anything (NaN included):
-        // zero those V rows before the tensor cores multiply them by P = 0.
+        // zero those V rows before the tensor cores multiply them by P = 0 (fp8: the
+        // dequant warps wrote them as zeros).
         const int k0 = ks + i * BN;
-        if (k0 + BN > kv_len) {
+        if (!F8 && k0 + BN > kv_len) {
           const int r_lo = max(0, kv_len - k0), r_hi = min(BN, ((kv_len + 15) & ~15) - k0);
           for (int e = lane; e < (r_hi - r_lo) * C::kCB * 8; e += 32) {
             const int r = r_lo + e / (C::kCB * 8), c = e % (C::kCB * 8);
@@ -312,6 +346,81 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     // nothing may still be in flight on the tensor cores when the memory is freed
     umma_commit_warp(fin);
     mbar_wait_bounded(fin, 0, p.status, DEV_TIMEOUT);
+  } else if (F8 && warp >= kDeq0) {
+    // ======================================================== fp8 dequant warps (thread = row)
+    // Q (bf16) to f16 in place once; then per key tile, K and V: the staging tile of codes
+    // (128-byte swizzled rows) into the f16 ring slot (two 128-byte swizzled column blocks
+    // a row), each e4m3 value exactly; V rows of keys at or past kv_len become zeros.
+    const int td = (warp - kDeq0) * 32 + lane;  // row of a tile
+    bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
+    if (ok && p.q_dtype == UA_DT_BF16) {
+#pragma unroll 1
+      for (int qt = 0; qt < NQ; ++qt)
+#pragma unroll 1
+        for (int cb = 0; cb < C::kCB; ++cb) {
+          uint4* row = reinterpret_cast<uint4*>(sQ + qt * C::kQBytes + cb * C::kBM * 128 + td * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // element-wise, so the chunk order does not matter
+            uint4 v = row[c];
+            v.x = pack_f16(bf16_lo(v.x), bf16_hi(v.x));
+            v.y = pack_f16(bf16_lo(v.y), bf16_hi(v.y));
+            v.z = pack_f16(bf16_lo(v.z), bf16_hi(v.z));
+            v.w = pack_f16(bf16_lo(v.w), bf16_hi(v.w));
+            row[c] = v;
+          }
+        }
+    }
+    fence_proxy_async_smem();  // generic writes, read by the tensor cores
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_ready);
+#pragma unroll 1
+    for (int j = 0; ok && j < nt; ++j) {
+#pragma unroll 1
+      for (int op = 0; op < 2; ++op) {
+        const int R = op ? RV : RK;
+        uint64_t* const f8_full = op ? v8_full : k8_full;
+        uint64_t* const f8_empty = op ? v8_empty : k8_empty;
+        if (!pf_wait_warp(f8_full, j & 1, abort_flag, p.status)) { ok = false; break; }
+        // take the row of codes into registers and hand the staging tile back at once, so
+        // the next tile's copy overlaps the conversion
+        const uint32_t sw = td & 7;
+        uint4 raw[8];
+        {
+          const uint8_t* src = (op ? sV8 : sK8) + td * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(f8_empty);
+        if (j >= R && !pf_wait_warp(&(op ? v_empty : k_empty)[j % R], ((j / R) - 1) & 1,
+                                    abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = (op ? sV : sK) + (j % R) * C::kTileBytes + td * 128;
+        const bool zero = op == 1 && ks + j * BN + td >= kv_len;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16 codes of the row -> f16 chunks 2c, 2c + 1
+          const uint4 r = zero ? make_uint4(0, 0, 0, 0) : raw[c];
+          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            h[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q]));
+            h[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16));
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int cc = 2 * c + u;  // f16 chunk of the row: column block cc / 8
+            *reinterpret_cast<uint4*>(dst + (cc >> 3) * C::kKVCB + (((cc & 7) ^ sw) << 4)) =
+                make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&(op ? v_full : k_full)[j % R]);
+      }
+    }
   } else {
     // ======================================================== softmax warps (thread = row)
     const int qt = warp >> 2;                              // q tile of this warp
@@ -345,7 +454,10 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     // With no softcap or bias the log2-domain score is c * s with c = scale * log2(e) > 0:
     // the row max is taken on the raw dot products and the scale folds into the exponent's
     // FMA.  Otherwise scores are transformed first and c = log2(e).
-    const float c = FEAT ? kLog2e : p.scale * kLog2e;
+    // fp8: the per-tensor k_scale joins the score scale, v_scale the output
+    const float kq = F8 ? p.scale * __ldg(p.kv_scale) : p.scale;
+    const float v_mul = F8 ? __ldg(p.kv_scale + 1) : 1.f;
+    const float c = FEAT ? kLog2e : kq * kLog2e;
     const bool sink = p.sinks != nullptr && z == 0 && rv;
     float m_used = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
     float l = sink ? 1.f : 0.f;
@@ -357,7 +469,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     // partition mask
     auto score = [&](float v, int jk, auto mask) -> float {
       if constexpr (FEAT) {
-        v *= p.scale;
+        v *= kq;
         if (p.softcap > 0.f) v = p.softcap * fast_tanh(v * inv_softcap);
         v += slope * static_cast<float>(jk - ctx);
         if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
@@ -486,7 +598,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
     if (ok) {
       const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
       const size_t n_part = static_cast<size_t>(p.n_part);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? v_mul / l : 0.f;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t rr[32];
@@ -528,8 +640,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
           float4* dst = reinterpret_cast<float4*>(p.ws_acc + w * D + c0);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
-                                 __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+            dst[e] = make_float4(__uint_as_float(rr[4 * e]) * v_mul, __uint_as_float(rr[4 * e + 1]) * v_mul,
+                                 __uint_as_float(rr[4 * e + 2]) * v_mul, __uint_as_float(rr[4 * e + 3]) * v_mul);
         }
       }
     }
@@ -540,10 +652,10 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ>::kThreads, 1)
   if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D, int NQ, bool BF16, bool FEAT>
+template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
 cudaError_t launch_prefill_tm_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
-  using C = PrefillTmCfg<D, NQ>;
-  auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT>;
+  using C = PrefillTmCfg<D, NQ, F8>;
+  auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT, F8>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -566,6 +678,11 @@ cudaError_t launch_prefill_tm_nq(const PrefillParams& pp, dim3 grid, int kv, boo
   if (kv == KV_F16)
     return feat ? launch_prefill_tm_t<D, NQ, false, true>(pp, grid, s)
                 : launch_prefill_tm_t<D, NQ, false, false>(pp, grid, s);
+  if constexpr (D == 128) {
+    if (kv == KV_E4M3)
+      return feat ? launch_prefill_tm_t<D, NQ, false, true, true>(pp, grid, s)
+                  : launch_prefill_tm_t<D, NQ, false, false, true>(pp, grid, s);
+  }
   return cudaErrorInvalidValue;
 }
 
