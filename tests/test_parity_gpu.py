@@ -62,7 +62,8 @@ def test_workload_parity_16bit_out(spec):
     assert (np.abs(got - want) <= bound).all()
 
 
-@pytest.mark.parametrize("spec", [W.PREFILL_D128, W.PREFILL_D256], ids=lambda s: s.name)
+@pytest.mark.parametrize("spec", [W.PREFILL_D128, W.PREFILL_D128_FP8, W.PREFILL_D256],
+                         ids=lambda s: s.name)
 def test_long_prefill_sampled_rows(spec):
     """Full-size prefill in the bench's launch configuration; sampled rows vs the oracle."""
     inp = W.make(spec)

@@ -223,7 +223,7 @@ def make(spec: Spec, *, poison: bool = False, replicas: int = 1) -> Inputs:
                   v_scale_tok=v_tok)
 
 
-# --- the five workloads ------------------------------------------------------------
+# --- the workloads ----------------------------------------------------------------
 
 TINY = Spec("tiny_fp16", [(1, 37), (5, 18)], 4, 2, 64, block_size=16, num_blocks=8, seed=0,
             desc="2 seqs (1,37),(5,18); 4q/2kv; d64; bs16; 8 physical blocks; causal")
@@ -243,12 +243,15 @@ SWDECODE_FP8_TOK = replace(SWDECODE_FP8, name="swdecode_fp8_tok", per_token_scal
 PREFILL_D128 = Spec("prefill_d128", [(4096, 4096)] * 4 + [(2048, 18432)], 32, 8, 128,
                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=4,
                     desc="4x4096 prompts + 2048 chunk behind 16384 prefix; 32q/8kv d128; bf16")
+PREFILL_D128_FP8 = replace(PREFILL_D128, name="prefill_d128_fp8", kv_dtype=torch.float8_e4m3fn,
+                           desc="4x4096 prompts + 2048 chunk behind 16384 prefix; 32q/8kv d128; "
+                                "bf16 q, fp8 e4m3 KV")
 PREFILL_D256 = replace(PREFILL_D128, name="prefill_d256", num_q_heads=24, num_kv_heads=4,
                        head_dim=256,
                        desc="4x4096 prompts + 2048 chunk behind 16384 prefix; 24q/4kv d256; bf16")
 
 WORKLOADS = {s.name: s for s in (TINY, DECODE, MIXED, SWDECODE_BF16, SWDECODE_FP8,
-                                 SWDECODE_FP8_TOK, PREFILL_D128, PREFILL_D256)}
+                                 SWDECODE_FP8_TOK, PREFILL_D128, PREFILL_D128_FP8, PREFILL_D256)}
 
 
 def kv_bytes_read(inp: Inputs) -> int:
