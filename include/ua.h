@@ -126,7 +126,8 @@ typedef struct {
                           64 or 256, block sizes not a multiple of 16); 8: tensor-memory
                           (tcgen05) kernel with 128-row q-blocks of floor(128 / G) tokens x
                           G heads (16-bit caches, or fp8 at head_dim 128: codes dequantised
-                          to f16 in shared memory, a bf16 q taken as f16); 16: the same
+                          to f16 in shared memory as in RocKE "fp8 KV cache", a bf16 q
+                          taken as f16); 16: the same
                           kernel with two such tiles of consecutive tokens per CTA */
   int32_t block_m;     /* (query token x head) rows per q-block */
   int32_t n_part;      /* key-range partitions (1 on the 2D path) */
