@@ -153,15 +153,13 @@ def test_dispatcher_decode_kernels():
 def test_dispatcher_prefill_kernels():
     prefill = dict(num_seqs=5, total_q=18432, max_seqlen_q=4096, max_seqlen_k=18432,
                    window_left=-1, max_blocks_per_seq=1152, num_blocks=6000)
-    # 16-bit caches, and fp8 at head_dim 128: the tensor-memory kernel, two q tiles a CTA
-    # when the grid still fills the device
+    # 16-bit caches, and fp8 at head_dim 64 and 128: the tensor-memory kernel, two q tiles
+    # a CTA when the grid still fills the device
     for kv in (_lib.UA_DT_BF16, _lib.UA_DT_F16, _lib.UA_DT_F8E4M3):
-        p = _plan(kv_dtype=kv, **prefill)
-        assert p["kernel"] == 16 and p["block_m"] == 2 * 128, kv
-        if kv != _lib.UA_DT_F8E4M3:
-            assert _plan(kv_dtype=kv, head_dim=64, **prefill)["kernel"] == 16
-    # fp8 at head_dim 64 or 256: the 64-row tile kernel
-    assert _plan(kv_dtype=_lib.UA_DT_F8E4M3, head_dim=64, **prefill)["kernel"] == 4
+        for d in (64, 128):
+            p = _plan(kv_dtype=kv, head_dim=d, **prefill)
+            assert p["kernel"] == 16 and p["block_m"] == 2 * 128, (kv, d)
+    # fp8 at head_dim 256: the 64-row tile kernel
     assert _plan(kv_dtype=_lib.UA_DT_F8E4M3, head_dim=256, **prefill)["kernel"] == 4
     assert _plan(kv_dtype=_lib.UA_DT_BF16, head_dim=256, **prefill)["kernel"] == 8
 

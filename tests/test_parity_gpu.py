@@ -117,14 +117,21 @@ SMALL = {
                                   qq_bias=True, qq_bias_shape=(64, 64), sinks=True),
     "pf_f16_g6_chunk": dict(seqs=[(70, 600), (1, 17)], num_q_heads=12, num_kv_heads=2,
                             window=300),
-    # fp8 caches on the tensor-memory kernel (head_dim 128): codes dequantised to f16 tiles
-    # in shared memory, a bf16 q converted to f16; one and two q tiles a CTA
+    # fp8 caches on the tensor-memory kernel (head_dim 64 and 128): codes dequantised to f16
+    # tiles in shared memory, a bf16 q converted to f16; one and two q tiles a CTA
     "pf_fp8_bf16q_window_sinks": dict(seqs=[(200, 500), (129, 129), (1, 300), (37, 45)],
                                       num_q_heads=32, num_kv_heads=8, q_dtype=torch.bfloat16,
                                       kv_dtype=torch.float8_e4m3fn, window=150, sinks=True),
     "pf_fp8_f16q_g16_feat": dict(seqs=[(150, 600), (9, 9)], num_q_heads=16, num_kv_heads=1,
                                  kv_dtype=torch.float8_e4m3fn, softcap=30.0, alibi=True,
                                  qq_bias=True, qq_bias_shape=(160, 160), sinks=True),
+    "pf_fp8_d64_g8_feat": dict(seqs=[(300, 700), (1, 65), (130, 130)], num_q_heads=16,
+                               num_kv_heads=2, head_dim=64, block_size=32,
+                               kv_dtype=torch.float8_e4m3fn, softcap=25.0, alibi=True,
+                               sinks=True, window=200),
+    "pf_fp8_d64_bf16q_mha": dict(seqs=[(200, 333), (64, 64)], num_q_heads=4, num_kv_heads=4,
+                                 head_dim=64, q_dtype=torch.bfloat16,
+                                 kv_dtype=torch.float8_e4m3fn),
     "pf_fp8_bf16q_two_tiles": dict(seqs=[(1500, 1500), (1000, 1600), (300, 300)],
                                    num_q_heads=32, num_kv_heads=8, block_size=32,
                                    q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,

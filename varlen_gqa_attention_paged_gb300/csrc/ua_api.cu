@@ -144,7 +144,7 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
   const long long rows_max = static_cast<long long>(sh->max_seqlen_q) * group;
   const bool tc = allow_tc && rows_max > 16 && group <= 128 && block_size % 16 == 0 &&
                   (kv_dtype == UA_DT_F16 || kv_dtype == UA_DT_BF16 ||
-                   (kv_dtype == UA_DT_F8E4M3 && d == 128));
+                   (kv_dtype == UA_DT_F8E4M3 && d <= 128));
   // decode with at most 8 rows per kv-head: the key-major decode tile (page boxes)
   const bool dec = allow_dec && !tc && rows_max <= 8 && d <= 128 && block_size % 16 == 0 &&
                    static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;

@@ -29,7 +29,7 @@
 // each operand in its own ring, 128-byte swizzled), warp 4NQ+2 MMA issuer and
 // tensor-memory owner.
 //
-// fp8-e4m3 caches (F8, head_dim 128): the producers copy fp8 K and V tiles into a staging
+// fp8-e4m3 caches (F8, head_dim 64 or 128): the producers copy fp8 K and V tiles into a staging
 // buffer, and four more warps (thread = row) turn each into the f16 tile the MMA reads
 // (every e4m3 value is an f16; V rows past kv_len become zeros), after converting a bf16
 // Q to f16 in place once; the MMAs and the softmax then run the f16 path, with k_scale
@@ -59,8 +59,8 @@ struct PrefillTmCfg {
   static constexpr int kKVCB = kBN * 128;                // one column block of a K or V tile
   static constexpr int kTileBytes = kCB * kKVCB;         // one K (or V) tile
   static constexpr int kBarBytes = 512;
-  // fp8 caches: one staging tile of fp8 codes per operand (128 keys x 128 bytes)
-  static constexpr int kF8Tile = kBN * 128;
+  // fp8 caches: one staging tile of fp8 codes per operand (128 keys x D bytes)
+  static constexpr int kF8Tile = kBN * D;
   static constexpr int kF8Bytes = F8 ? 2 * kF8Tile : 0;
   static constexpr int kDeqWarps = F8 ? 4 : 0;
   // K and V ring depths: as many tiles as fit beside Q (K gets the odd one, at most 4 each)
@@ -78,7 +78,7 @@ struct PrefillTmCfg {
   static_assert(NQ * kTmemStride <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kRingK >= 2 && kRingV >= 2, "at least double-buffered K and V");
-  static_assert(!F8 || D == 128, "fp8 caches: head_dim 128 (one 128-byte column block of codes)");
+  static_assert(!F8 || D == 64 || D == 128, "fp8 caches: head_dim 64 or 128");
 };
 
 template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
     uint64_t* const empty = F8 ? (is_k ? k8_empty : v8_empty) : (is_k ? k_empty : v_empty);
     uint8_t* const ring = F8 ? (is_k ? sK8 : sV8) : (is_k ? sK : sV);
     constexpr int kTileIn = F8 ? C::kF8Tile : C::kTileBytes;  // bytes of one copied tile
-    constexpr int kCBIn = F8 ? 1 : C::kCB;                     // its 128-byte column blocks
+    constexpr int kCBIn = F8 ? 1 : C::kCB;                     // its column blocks
+    constexpr int kBoxIn = F8 ? 16 * D : 2048;                 // one page box (16 rows)
     const CUtensorMap* const map = is_k ? &pp.tmap_k : &pp.tmap_v;
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
     const int bs = p.block_size;
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
       if (lane < BN / 16)
 #pragma unroll
         for (int cb = 0; cb < kCBIn; ++cb)
-          tma_load_3d_pf(ring + sl * kTileIn + cb * C::kKVCB + lane * 2048, map, 64 * cb, g,
+          tma_load_3d_pf(ring + sl * kTileIn + cb * C::kKVCB + lane * kBoxIn, map, 64 * cb, g,
                          row, &full[sl]);
       issued = j + 1;
     }
@@ -349,8 +350,9 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
   } else if (F8 && warp >= kDeq0) {
     // ======================================================== fp8 dequant warps (thread = row)
     // Q (bf16) to f16 in place once; then per key tile, K and V: the staging tile of codes
-    // (128-byte swizzled rows) into the f16 ring slot (two 128-byte swizzled column blocks
-    // a row), each e4m3 value exactly; V rows of keys at or past kv_len become zeros.
+    // (D-byte rows: 128-byte swizzled at d128, plain at d64) into the f16 ring slot
+    // (128-byte swizzled column blocks), each e4m3 value exactly; V rows of keys at or past
+    // kv_len become zeros.
     const int td = (warp - kDeq0) * 32 + lane;  // row of a tile
     bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
     if (ok && p.q_dtype == UA_DT_BF16) {
@@ -360,7 +362,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
         for (int cb = 0; cb < C::kCB; ++cb) {
           uint4* row = reinterpret_cast<uint4*>(sQ + qt * C::kQBytes + cb * C::kBM * 128 + td * 128);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {  // element-wise, so the chunk order does not matter
+          for (int c0 = 0; c0 < 8; ++c0) {  // element-wise: the order only spreads the banks
+            const int c = c0 ^ (td & 7);
             uint4 v = row[c];
             v.x = pack_f16(bf16_lo(v.x), bf16_hi(v.x));
             v.y = pack_f16(bf16_lo(v.y), bf16_hi(v.y));
@@ -383,12 +386,21 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
         if (!pf_wait_warp(f8_full, j & 1, abort_flag, p.status)) { ok = false; break; }
         // take the row of codes into registers and hand the staging tile back at once, so
         // the next tile's copy overlaps the conversion
+        // 16-code chunk c of the loop is chunk cs(c) of the row.  At d64 (64-byte rows, two
+        // to a bank line) the order turns with the row pair a = td / 2 % 4 by pi(a) (pi =
+        // 0, 2, 3, 1: pi(a) and pi(a) ^ a both permute 0..3), so the eight rows of a quarter
+        // warp hit eight distinct 16-byte bank groups in the loads and in the stores.
+        constexpr int kCh = D / 16;
         const uint32_t sw = td & 7;
-        uint4 raw[8];
+        const int rot = D == 128 ? 0 : (0x78 >> (2 * ((td >> 1) & 3))) & 3;
+        auto cs = [&](int c) -> int { return c ^ rot; };
+        uint4 raw[kCh];
         {
-          const uint8_t* src = (op ? sV8 : sK8) + td * 128;
+          const uint8_t* src = (op ? sV8 : sK8) + td * D;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+          for (int c = 0; c < kCh; ++c)
+            raw[c] = *reinterpret_cast<const uint4*>(
+                src + ((D == 128 ? (cs(c) ^ sw) : cs(c)) << 4));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(f8_empty);
@@ -400,7 +412,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
         uint8_t* dst = (op ? sV : sK) + (j % R) * C::kTileBytes + td * 128;
         const bool zero = op == 1 && ks + j * BN + td >= kv_len;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16 codes of the row -> f16 chunks 2c, 2c + 1
+        for (int c = 0; c < kCh; ++c) {  // 16 codes of the row -> f16 chunks 2cs, 2cs + 1
           const uint4 r = zero ? make_uint4(0, 0, 0, 0) : raw[c];
           const uint32_t w[4] = {r.x, r.y, r.z, r.w};
           uint32_t h[8];
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
           }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int cc = 2 * c + u;  // f16 chunk of the row: column block cc / 8
+            const int cc = 2 * cs(c) + u;  // f16 chunk of the row: column block cc / 8
             *reinterpret_cast<uint4*>(dst + (cc >> 3) * C::kKVCB + (((cc & 7) ^ sw) << 4)) =
                 make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
           }
@@ -678,11 +690,9 @@ cudaError_t launch_prefill_tm_nq(const PrefillParams& pp, dim3 grid, int kv, boo
   if (kv == KV_F16)
     return feat ? launch_prefill_tm_t<D, NQ, false, true>(pp, grid, s)
                 : launch_prefill_tm_t<D, NQ, false, false>(pp, grid, s);
-  if constexpr (D == 128) {
-    if (kv == KV_E4M3)
-      return feat ? launch_prefill_tm_t<D, NQ, false, true, true>(pp, grid, s)
-                  : launch_prefill_tm_t<D, NQ, false, false, true>(pp, grid, s);
-  }
+  if (kv == KV_E4M3)
+    return feat ? launch_prefill_tm_t<D, NQ, false, true, true>(pp, grid, s)
+                : launch_prefill_tm_t<D, NQ, false, false, true>(pp, grid, s);
   return cudaErrorInvalidValue;
 }
 
