@@ -123,9 +123,9 @@ typedef struct {
                           2: key-major decode tile, 8 rows per CTA (decode with at most 8
                           rows per kv-head, head_dim <= 128, 16 | block_size);
                           4: warp-MMA tile kernel, 64 rows per CTA (fp8 caches at head_dim
-                          64 or 256, block sizes not a multiple of 16); 8: tensor-memory
+                          256, block sizes not a multiple of 16); 8: tensor-memory
                           (tcgen05) kernel with 128-row q-blocks of floor(128 / G) tokens x
-                          G heads (16-bit caches, or fp8 at head_dim 128: codes dequantised
+                          G heads (16-bit caches, or fp8 at head_dim <= 128: codes dequantised
                           to f16 in shared memory as in RocKE "fp8 KV cache", a bf16 q
                           taken as f16); 16: the same
                           kernel with two such tiles of consecutive tokens per CTA */
