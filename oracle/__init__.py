@@ -7,7 +7,9 @@ CUDA library and never calls it; the product path never calls the oracle.
 The arithmetic lives in ``ua_ref.c`` (one output row at a time, by the plain
 definition, plus the split-KV form used to pin the partition/merge algorithm);
 this module only marshals arrays into it and spreads rows over host threads.
-Sources are cited in ``ua_ref.c``.
+Sources are cited in ``ua_ref.c``.  Parity unpinned: the order in which softcap and
+the ALiBi / QQ-bias terms compose (the pages name the terms, not their order); every
+term on its own is pinned.
 """
 from __future__ import annotations
 

@@ -39,7 +39,10 @@
  *   with kv_len < q_len whose position p is negative have no key).
  *
  *   The order "scale, softcap, ALiBi, QQ-bias, mask" is this library's reading of
- *   the pages, which name the terms but do not print their order.
+ *   the pages, which name the terms but do not print their order: parity unpinned
+ *   for the composition of softcap with the biases (each term alone is pinned by the
+ *   tests: closed forms, the row-shift invariance of ALiBi without sinks, softcap
+ *   limits, brute force).
  *
  * Element decoders follow the published bit layouts: IEEE-754 binary16, bfloat16
  * (upper half of binary32) and OCP 8-bit e4m3fn (bias 7, no infinities, S.1111.111
