@@ -3,6 +3,7 @@ bad arguments before touching the GPU, and the dispatcher plans as designed."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -28,6 +29,34 @@ def test_library_exports_every_declared_symbol():
     assert lib.ua_version() == 100
     assert lib.ua_status_string(0) == b"ok"
     assert b"workspace" in lib.ua_status_string(4)
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """Every field of ua_shape_t and ua_plan_t sits at the same offset, with the same size,
+    in the C compiler's layout of include/ua.h and in the ctypes mirrors of the binding."""
+    structs = {"ua_shape_t": _lib.UaShape, "ua_plan_t": _lib.UaPlan}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ua.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu %zu\\n", offsetof({cname}, {f}), '
+                         f"sizeof((({cname}*)0)->{f}));")
+    lines += ["return 0;", "}"]
+    src, exe = tmp_path / "layout.c", tmp_path / "layout"
+    src.write_text("\n".join(lines) + "\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(root, "include"), "-o", str(exe),
+                    str(src)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {}
+    for ln in out.splitlines():
+        parts = ln.split()
+        got[(parts[0], parts[1])] = tuple(int(x) for x in parts[2:])
+    for cname, py in structs.items():
+        assert got[(cname, "sizeof")] == (ctypes.sizeof(py),), cname
+        for f, _ in py._fields_:
+            desc = getattr(py, f)
+            assert got[(cname, f)] == (desc.offset, desc.size), (cname, f)
 
 
 FAKE = 0x7f0000001000  # aligned, never dereferenced: every case fails validation first
