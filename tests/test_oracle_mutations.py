@@ -38,6 +38,10 @@ MUTANTS = {
                                 "(int64_t)(j % P->block_size) * st[2]"),
     "token_scale_head_dropped": ("+ (int64_t)g * st[2]", "+ 0 * st[2]"),
     "slot_from_wrong_block": ("(size_t)(j % P->block_size)", "(size_t)((j + 1) % P->block_size)"),
+    "causal_excludes_self": ("*hi = p + 1 < kv_len ? p + 1 : kv_len;", "*hi = p < kv_len ? p : kv_len;"),
+    "qq_bias_skips_first_key": ("if (P->qq_bias && j >= ctx)", "if (P->qq_bias && j >= ctx + 1)"),
+    "e4m3_exponent_bias": ("else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "e4m3_subnormal_scale": ("if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp((double)m, -10);"),
 }
 
 PROBES = [
