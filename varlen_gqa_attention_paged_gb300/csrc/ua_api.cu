@@ -131,10 +131,11 @@ int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, in
 // Kernel: decode calls with at most 8 rows per kv-head, head_dim <= 128 and page-sized
 // TMA boxes take the key-major decode tile (keys on the MMA's M side, rows on N); other
 // decode-shaped calls (every sequence's rows fit 16) take the warp-MMA tile kernel with
-// 16-row q-blocks; other calls on fp16/bf16 caches with 16 | block_size take the
-// tensor-memory kernel with 128-row q tiles (floor(128 / G) tokens x G heads), two tiles
-// per CTA for head_dim <= 128 when that grid still fills the device; the rest (fp8
-// caches, other block sizes) take the tile kernel with 64-row q-blocks.
+// 16-row q-blocks; other calls with 16 | block_size (fp16/bf16 caches, or fp8 at head_dim
+// <= 128) take the tensor-memory kernel with 128-row q tiles (floor(128 / G) tokens x G
+// heads), two tiles per CTA for head_dim <= 128 when that grid still fills the device; the
+// rest (fp8 caches at head_dim 256, other block sizes) take the tile kernel with 64-row
+// q-blocks.
 bool is_tc(int kernel) { return kernel == ua::KERNEL_TC128 || kernel == ua::KERNEL_TC256; }
 
 void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int window_left,
