@@ -8,9 +8,9 @@
  * tables, cumulative query lengths, optional sliding window, softcap, sinks, ALiBi
  * slopes, QQ-bias).  The library chooses between two execution paths ("2D": one
  * CTA per q-block x kv-head walks every key; "split": the key range is cut into
- * partitions whose max / sum / partial output are merged by a second kernel, as in
- * the aiter PR #3962 "split-K long-context decode for shuffled fp8 SWA",
- * "Changes").
+ * partitions whose max / sum / partial output are merged, as in the aiter PR #3962
+ * "split-K long-context decode for shuffled fp8 SWA", "Changes" -- inside the
+ * thread-block cluster of a decode slot's partitions, or by a second kernel).
  *
  * Semantics, for sequence b with q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b],
  * kv_len = seq_lens_k[b] and ctx = kv_len - q_len, query row i (0 <= i < q_len)
@@ -21,6 +21,9 @@
  *   s_j += alibi_slopes[h] * (j - ctx)     if alibi_slopes != NULL
  *   s_j += qq_bias[i * qq_bias_stride + (j - ctx)]  if qq_bias != NULL and j >= ctx
  *   out  = sum_j e^{s_j} V_j / (e^{sinks[h]} (if sinks != NULL) + sum_j e^{s_j})
+ *                                      (fp8 cache: V_j = e4m3 * v_scale; per-token
+ *                                       scales, when given, replace k_scale / v_scale
+ *                                       key by key: see ua_shape_t)
  * A row with no allowed key (possible only when kv_len < q_len, e.g. a decode slot
  * with kv_len 0) is written as 0.
  *
