@@ -460,15 +460,9 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}.get(spec.kv_dtype, "f16 (e4m3 KV)"),
         "data": "synthetic (seeded N(0,1) q/k/v, shuffled block table)",
-        "config": {"workload": spec.name, "desc": spec.desc, "batch": len(spec.seqs),
-                   "q_len": spec.seqs[0][0], "kv_len": spec.seqs[0][1], "window": spec.window,
-                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
-                   "head_dim": spec.head_dim, "block_size": spec.block_size,
-                   "path": "split" if call.plan["path"] == 2 else "2d",
-                   "n_part": call.plan["n_part"],
-                   "l2": f"inputs larger than L2: {reps} cache replicas on disjoint blocks, "
-                         f"step i reads replica i mod {reps}",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(spec, world),
+        "plan": {"path": "split" if call.plan["path"] == 2 else "2d",
+                 "n_part": call.plan["n_part"], "kernel_code": call.plan["kernel"]},
         "hbm_gbs": round(kbytes * args.steps / (elapsed_ms * 1e-3) / 1e9, 1),
         "roofline": {**roof,
                      "traffic": recorded_traffic(kname, spec.name), "peak_source": peak_kind,
@@ -510,18 +504,41 @@ def run_launches(args):
                       "plan": call.plan}))
 
 
+def sample_heads(total_heads, threads, budget_heads):
+    """Heads of a CPU sample: a multiple of the thread count (or every head when there are
+    fewer heads than threads), within the budget, at least one round."""
+    if total_heads <= threads:
+        return total_heads
+    rounds = max(1, min(total_heads // threads, budget_heads // threads))
+    return rounds * threads
+
+
+def workload_config(spec, world):
+    """The `config` of both arms' JSON line: the workload and its input rule."""
+    reps = n_replicas(spec)
+    return {"workload": spec.name, "desc": spec.desc, "batch": len(spec.seqs),
+            "q_len": spec.seqs[0][0], "kv_len": spec.seqs[0][1], "window": spec.window,
+            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+            "head_dim": spec.head_dim, "block_size": spec.block_size,
+            "l2": f"inputs larger than L2: {reps} cache replicas on disjoint blocks, "
+                  f"step i reads replica i mod {reps}",
+            "parallelism": f"replicas x{world}"}
+
+
 def cpu_baseline(inp, budget_s=12.0, sample_seqs=None):
     """The oracle as it stands, on the host cores, over a bounded sample of the workload."""
     import oracle
     threads = os.cpu_count() or 1
     kw = inp.oracle_kwargs()
     total_heads = inp.spec.num_q_heads
-    # one sample = every query token of the step for a slice of heads, sized to ~1 s
-    heads = total_heads
+    # one sample = every query token of the step for a slice of heads, sized to ~1 s; the
+    # oracle runs one head per host thread, so the slice is a whole number of rounds of
+    # `threads` heads (no thread idles in a last, partial round)
     t0 = time.time()
     oracle.attention(threads=threads, head_range=(0, 1), **kw)
     one = max(time.time() - t0, 1e-3)
-    heads = max(1, min(total_heads, int(1.0 / one)))
+    heads = sample_heads(total_heads, threads, int(1.0 / one) * threads)
+    threads = min(threads, heads)
     done_tokens = 0.0
     t0 = time.time()
     reps = 0
@@ -552,9 +569,11 @@ def run_reference(args):
     t0 = time.time()
     oracle.attention(threads=threads, head_range=(0, 1), **kw)
     one = max(time.time() - t0, 1e-3)
-    # each step: all query tokens, a slice of heads sized so K+W steps take ~2 minutes
+    # each step: all query tokens, a slice of heads sized so K+W steps take ~2 minutes,
+    # a whole number of rounds of one head per thread
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    heads = max(1, min(total_heads, int(per_step_budget / one)))
+    heads = sample_heads(total_heads, threads, int(per_step_budget / one) * threads)
+    threads = min(threads, heads)
     for _ in range(args.warmup):
         oracle.attention(threads=threads, head_range=(0, heads), **kw)
     t0 = time.time()
@@ -570,7 +589,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) q/k/v, shuffled block table)",
-            "config": {"workload": spec.name, "desc": spec.desc},
+            "config": workload_config(spec, world),
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

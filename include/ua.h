@@ -196,7 +196,9 @@ int ua_unified_attention(const void* q, const void* k_cache, const void* v_cache
  *   - UA_ERR_SCRATCH_LIMIT, before anything is launched, when the plan needs more than
  *     UA_NOALLOC_SCRATCH_BYTES of scratch (ua_plan reports workspace_bytes).
  *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture on the device.
+ *     current); make that first call before any stream capture on the device.  The
+ *     address is kept until the process exits and does not survive cudaDeviceReset:
+ *     after a reset of the device, do not call this entry point again.
  *   - Every call on a device shares the one array: calls whose kernels overlap on the
  *     GPU (different streams, or several host threads) race on it and give wrong
  *     results.  Calls on one stream are ordered and safe.  The array keeps the last
@@ -224,7 +226,17 @@ int ua_plan(const ua_shape_t* shape, int block_size, int num_q_heads, int num_kv
             int head_dim, int window_left, int kv_dtype, int backend, int num_sms,
             ua_plan_t* plan);
 
-/* Workspace bytes the call with these sizes needs (0 when it takes the 2D path). */
+/*
+ * ua_workspace_bytes -- bytes of split-path scratch a call with these sizes needs on the
+ * current device (0 when it takes the 2D path or merges its partitions inside a
+ * thread-block cluster): fp32 max and sum per (query token, head, partition), then the
+ * unnormalised partial output rows, each piece 256-byte aligned.  The scratch rules follow
+ * the author's follow-up on the review of aiter PR #3962 ("split-K long-context decode for
+ * shuffled fp8 SWA"): the partition count is capped, the scratch belongs to one stream at a
+ * time (a caller workspace, or the library's own buffer per device and stream), and every
+ * entry the merge reads is written by the same call, so the scratch needs no clearing.
+ * Returns 0 on an invalid argument too.
+ */
 size_t ua_workspace_bytes(const ua_shape_t* shape, int block_size, int num_q_heads,
                           int num_kv_heads, int head_dim, int window_left, int kv_dtype,
                           int backend);
@@ -235,6 +247,11 @@ size_t ua_workspace_bytes(const ua_shape_t* shape, int block_size, int num_q_hea
  * UA_OK, UA_ERR_DEVICE_CHECK (a block id outside the cache, or a q_len
  * above max_seqlen_q in a decode-shaped call) or UA_ERR_TIMEOUT (a
  * bounded wait expired).  Returns UA_OK or UA_ERR_CUDA / UA_ERR_INVALID_ARG.
+ * The word reports what the kernels refuse to read rather than faulting: a bad block id
+ * is never dereferenced (its keys count as zero).  Slots of a sequence's last page at or
+ * past kv_len are never an input either: whatever they hold (NaN included) gets weight
+ * exactly 0 and its V values are zeroed before P.V, after the NaN-in-unused-V-slots
+ * finding of the follow-up on aiter PR #3962's review.
  */
 int ua_device_status(void* stream, int* status);
 

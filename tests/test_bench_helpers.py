@@ -78,3 +78,22 @@ def test_peaks_are_positive_and_name_their_source():
     hbm, tc, tc_sustained, src = bench.peaks()
     assert hbm > 0 and tc > 0 and tc_sustained > 0
     assert src in ("measured", "fallback")
+
+
+def test_cpu_sample_heads_are_whole_rounds_of_threads():
+    import bench
+    assert bench.sample_heads(32, 16, 19) == 16
+    assert bench.sample_heads(32, 16, 40) == 32
+    assert bench.sample_heads(32, 16, 1) == 16      # at least one round
+    assert bench.sample_heads(8, 16, 3) == 8        # fewer heads than threads: every head
+    assert bench.sample_heads(24, 16, 100) == 16    # never past the heads there are
+    for heads, threads, budget in ((32, 16, 19), (24, 8, 9), (16, 4, 13)):
+        assert bench.sample_heads(heads, threads, budget) % threads == 0
+
+
+def test_both_arms_share_one_config_dict():
+    import bench
+    import workloads as W
+    cfg = bench.workload_config(W.SWDECODE_BF16, 1)
+    assert cfg["workload"] == "swdecode_bf16" and "l2" in cfg
+    assert cfg == bench.workload_config(W.SWDECODE_BF16, 1)

@@ -62,25 +62,106 @@ def test_workload_parity_16bit_out(spec):
     assert (np.abs(got - want) <= bound).all()
 
 
-@pytest.mark.parametrize("spec", [W.PREFILL_D128, W.PREFILL_D128_FP8, W.PREFILL_D256],
-                         ids=lambda s: s.name)
-def test_long_prefill_sampled_rows(spec):
-    """Full-size prefill in the bench's launch configuration; sampled rows vs the oracle."""
-    inp = W.make(spec)
-    out = run(inp, backend="auto").cpu()
-    g = np.random.default_rng(0)
+def _plan(inp, backend="auto", num_splits=0):
+    """The dispatcher's decision for an input set on this device."""
+    spec = inp.spec
+    bt = inp.block_table if inp.block_table.dim() == 2 else inp.block_table[0]
+    return ua.plan(num_seqs=inp.num_seqs, total_q=inp.total_q, max_seqlen_q=inp.max_seqlen_q,
+                   max_seqlen_k=inp.max_seqlen_k, block_size=spec.block_size,
+                   num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                   head_dim=spec.head_dim, window_left=inp.window_left,
+                   kv_dtype=ua._DTYPES[spec.kv_dtype], q_dtype=ua._DTYPES[spec.q_dtype],
+                   backend=backend, num_splits=num_splits, max_blocks_per_seq=bt.shape[-1],
+                   num_blocks=inp.k_cache.shape[0])
+
+
+def _tile_rows(inp, tokens_per_tile, tiles_per_seq=64):
+    """(token, head) rows of every head for the first and last token of `tiles_per_seq`
+    q tiles of each sequence, spread from the first tile to the last (both parities of
+    the tile index, so both tiles of a two-tile CTA)."""
     cu = inp.cu_seqlens_q.tolist()
     tok = []
     for b in range(inp.num_seqs):
         a, e = cu[b], cu[b + 1]
-        tok += [a, a + 1, e - 1, e - 2] + list(g.integers(a, e, size=6))
-    tok = np.array(tok, dtype=np.int32)
-    heads = g.integers(0, spec.num_q_heads, size=len(tok)).astype(np.int32)
+        n = (e - a + tokens_per_tile - 1) // tokens_per_tile
+        for t in sorted(set(np.linspace(0, n - 1, min(n, tiles_per_seq)).round().astype(int))):
+            first = a + t * tokens_per_tile
+            tok += [first, min(e, first + tokens_per_tile) - 1]
+    hq = inp.spec.num_q_heads
+    tok = np.repeat(np.array(tok, dtype=np.int32), hq)
+    heads = np.tile(np.arange(hq, dtype=np.int32), len(tok) // hq)
+    # shuffled, so the oracle's threads get rows of every sequence (and cost) alike
+    perm = np.random.default_rng(0).permutation(len(tok))
+    return tok[perm], heads[perm]
+
+
+@pytest.mark.parametrize("spec,kernel", [(W.PREFILL_D128, 16), (W.PREFILL_D128_FP8, 16),
+                                         (W.PREFILL_D256, 8)],
+                         ids=["prefill_d128", "prefill_d128_fp8", "prefill_d256"])
+def test_long_prefill_sampled_rows(spec, kernel):
+    """Full-size prefill in the bench's launch configuration: every head of the first and
+    last token of 64 q tiles per sequence (over 15,000 rows) against the oracle, for the
+    fp32 output and for the 16-bit output (the oracle's row rounded, plus the bar)."""
+    inp = W.make(spec)
+    assert _plan(inp)["kernel"] == kernel
+    out = run(inp, backend="auto").cpu()
+    out16 = run(inp, backend="auto", out_dtype=spec.q_dtype).cpu()
+    assert torch.isfinite(out).all() and torch.isfinite(out16.float()).all()
+    tq = 128 // (spec.num_q_heads // spec.num_kv_heads)
+    tok, heads = _tile_rows(inp, tq)
+    assert len(tok) >= 4000
     want = oracle.attention_rows(tokens=tok, heads=heads, threads=THREADS, **inp.oracle_kwargs())
-    got = out[torch.from_numpy(tok).long(), torch.from_numpy(heads).long()].double().numpy()
+    ti, hi = torch.from_numpy(tok).long(), torch.from_numpy(heads).long()
+    got = out[ti, hi].double().numpy()
     err = float(np.abs(got - want).max())
     assert err <= TOL[spec.kv_dtype], f"max abs err {err:.3e}"
-    assert torch.isfinite(out).all()
+    got16 = out16[ti, hi].double().numpy()
+    bound = TOL[spec.kv_dtype] + ulp16(want, spec.q_dtype)
+    assert (np.abs(got16 - want) <= bound).all()
+
+
+# Two 128-row q tiles a CTA with a 16-bit cache (plan kernel code 16, the kernel the long
+# prefill bench times): enough tokens that the halved grid still fills the device, with
+# the window and sinks, every score feature at G = 16, head_dim 64, ragged sequence ends.
+TWO_TILE = {
+    "pf2_bf16_window_sinks": dict(seqs=[(1500, 1500), (1000, 1600), (300, 300)],
+                                  num_q_heads=32, num_kv_heads=8, q_dtype=torch.bfloat16,
+                                  kv_dtype=torch.bfloat16, window=256, sinks=True),
+    "pf2_f16_g16_feat": dict(seqs=[(1500, 1700), (1300, 1300)], num_q_heads=16,
+                             num_kv_heads=1, softcap=30.0, alibi=True, qq_bias=True,
+                             qq_bias_shape=(1500, 1500), sinks=True),
+    "pf2_bf16_d64_g8_bs32": dict(seqs=[(1000, 1200), (700, 700), (65, 65)], num_q_heads=32,
+                                 num_kv_heads=4, head_dim=64, block_size=32,
+                                 q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16),
+    "pf2_f16_chunk_behind_prefix": dict(seqs=[(1200, 5000), (1100, 1100), (7, 7)],
+                                        num_q_heads=32, num_kv_heads=8, window=700),
+}
+
+
+def _two_tile_inputs(case):
+    key = "two_tile/" + case
+    if key not in _INPUT_CACHE:
+        kw = dict(head_dim=128, seed=200 + sorted(TWO_TILE).index(case))
+        kw.update(TWO_TILE[case])
+        spec = W.Spec(name=case, **kw)
+        _INPUT_CACHE[key] = W.make(spec, poison=True)
+    return _INPUT_CACHE[key]
+
+
+@pytest.mark.parametrize("backend", ["auto", "2d", "split"])
+@pytest.mark.parametrize("case", sorted(TWO_TILE))
+def test_two_tile_prefill_16bit_cache(case, backend):
+    inp = _two_tile_inputs(case)
+    assert _plan(inp, backend)["kernel"] == 16, "the case must reach the two-tile kernel"
+    want = oracle_out(inp, "two_tile/" + case)
+    out = run(inp, backend=backend)
+    err = max_err(out, want)
+    assert err <= TOL[inp.spec.kv_dtype], f"{case}/{backend}: {err:.3e}"
+    if backend == "auto":
+        out16 = run(inp, backend=backend, out_dtype=inp.spec.q_dtype)
+        got = out16.cpu().to(torch.float64).numpy()
+        bound = TOL[inp.spec.kv_dtype] + ulp16(want, inp.spec.q_dtype)
+        assert (np.abs(got - want) <= bound).all()
 
 
 def _small(seed, **kw):

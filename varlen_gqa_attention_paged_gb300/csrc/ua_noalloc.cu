@@ -13,6 +13,8 @@
 // shares it.  Its host-side name is only a stand-in for the device array: host code
 // must not hand it to a kernel.  The device address comes from cudaGetSymbolAddress,
 // looked up once per device, with that device current, by the first call made on it.
+// The looked-up address is kept for the life of the process: it does not survive a
+// cudaDeviceReset of that device (after one, this entry point must not be called again).
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -66,10 +68,14 @@ extern "C" int ua_unified_attention_noalloc(
     ua_shape_t sh = *shape;
     sh.workspace = scratch;
     sh.workspace_bytes = kScratchBytes;
-    return ua_unified_attention(q, k_cache, v_cache, out, cu_seqlens_q, seq_lens_k, block_table,
-                                block_size, num_q_heads, num_kv_heads, head_dim, scale, softcap,
-                                window_left, alibi_slopes, qq_bias, sinks, kv_dtype, kv_scale,
-                                backend, stream, &sh);
+    rc = ua_unified_attention(q, k_cache, v_cache, out, cu_seqlens_q, seq_lens_k, block_table,
+                              block_size, num_q_heads, num_kv_heads, head_dim, scale, softcap,
+                              window_left, alibi_slopes, qq_bias, sinks, kv_dtype, kv_scale,
+                              backend, stream, &sh);
+    // The call plans again for another kernel when a tensor map cannot be encoded; if that
+    // plan needs more scratch than the array, the inner call reports a short workspace,
+    // which for this entry point means the fixed array is too small.
+    return rc == UA_ERR_WORKSPACE ? UA_ERR_SCRATCH_LIMIT : rc;
   } catch (...) {
     return UA_ERR_CUDA;
   }
