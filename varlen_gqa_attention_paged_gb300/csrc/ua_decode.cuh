@@ -71,7 +71,8 @@ struct DecCfg {
   }
 };
 
-template <int D, int KV, bool FEAT>
+// QT: e4m3 terms of Q for fp8 caches (2 for a bf16 q, 3 for an f16 q); unused otherwise.
+template <int D, int KV, bool FEAT, int QT>
 __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
     ua_decode_kernel(const __grid_constant__ TileParams tp) {
   using C = DecCfg<D, KV>;
@@ -248,7 +249,6 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
     }
   }
   const float scale = p.scale * k_scale;
-  const float scale_log2 = scale * kLog2e;
 
   // The accumulator rows of this lane: 2cq and 2cq + 1 (N columns of the S^T / O^T tiles).
   bool rv[2];
@@ -271,28 +271,98 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
 
   // Q^T fragments (B operand, 16 d x 8 rows): column gq of the tile is row gq of the
   // q-block; lane cq holds d 2cq, 2cq + 1 (register 0) and 2cq + 8, 2cq + 9 (register 1)
-  // of each 16-d slice, in the MMA input type.  fp8: slice kk of lane cq is
-  // d = cq D/4 + 4 kk + {0..3}, the K bytes the lane reads.
-  uint32_t qt[D / 16][2];
+  // of each 16-d slice, in the MMA input type (16-bit caches).
+  //
+  // fp8 caches: the QK product runs on the e4m3 tensor-core MMA straight from the cached
+  // codes, so Q^T becomes e4m3 too, without losing precision: row gq is scaled by a power
+  // of two 2^c that puts its largest magnitude in [128, 256), and written as the sum of QT
+  // e4m3 terms (a 16-bit value's significand is the sum of its first two (bf16: 8 bits) or
+  // three (f16: 11 bits) 4-bit pieces, each a normal e4m3 value in that range; pieces below
+  // e4m3's smallest subnormal, 2^-9, are lost: under 2^-17 of the row's largest value).
+  // Lane cq holds d = cq D/4 + 8t + {0..3} (b0) and + {4..7} (b1) of k-step t, the bytes of
+  // the K rows it reads; the score then takes the factor 2^-c back.
+  constexpr int kQT = C::kPermD ? QT : 1;
+  uint32_t qt[C::kPermD ? 1 : D / 16][2];
+  uint32_t q8[kQT][C::kPermD ? D / 32 : 1][2];
+  float row_scale[2] = {1.f, 1.f};  // 2^-c of rows 2cq and 2cq + 1 (fp8)
   {
     const bool qv = gq < nr && q0 + gq / G < p.total_q;
     const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
                            (static_cast<size_t>(q0 + (qv ? gq / G : 0)) * p.hq + g * G +
                             (qv ? gq % G : 0)) *
                                D;
+    if constexpr (!C::kPermD) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int col = C::kPermD ? cq * (D / 4) + 4 * kk + 2 * h : kk * 16 + 2 * cq + 8 * h;
-        uint32_t v = qv ? __ldg(reinterpret_cast<const unsigned int*>(qrow + col)) : 0u;
-        if constexpr (KV == KV_E4M3) {
-          if (p.q_dtype == UA_DT_BF16) v = pack_f16(bf16_lo(v), bf16_hi(v));
+        for (int h = 0; h < 2; ++h) {
+          const int col = kk * 16 + 2 * cq + 8 * h;
+          qt[kk][h] = qv ? __ldg(reinterpret_cast<const unsigned int*>(qrow + col)) : 0u;
         }
-        qt[kk][h] = v;
       }
+    } else {
+      constexpr int kN = D / 4;  // values of row gq this lane holds
+      float x[kN];
+#pragma unroll
+      for (int i = 0; i < kN; i += 8) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (qv) w = __ldg(reinterpret_cast<const uint4*>(qrow + cq * kN + i));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (p.q_dtype == UA_DT_BF16) {
+            x[i + 2 * k] = bf16_lo(ww[k]);
+            x[i + 2 * k + 1] = bf16_hi(ww[k]);
+          } else {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
+            x[i + 2 * k] = f.x;
+            x[i + 2 * k + 1] = f.y;
+          }
+        }
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < kN; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      // amax in [2^(E-127), 2^(E-126)) with E its biased exponent: c = 134 - E puts it in
+      // [128, 256); c stays inside the normal range of fp32 powers of two
+      const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+      const int c = min(126, max(-126, 134 - ebits));
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + c) << 23);
+      const float down = __uint_as_float(static_cast<uint32_t>(127 - c) << 23);
+#pragma unroll
+      for (int i = 0; i < kN; ++i) x[i] *= up;
+#pragma unroll
+      for (int term = 0; term < kQT; ++term) {
+#pragma unroll
+        for (int t = 0; t < D / 32; ++t) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int d0 = 8 * t + 4 * h;
+            const uint32_t c01 = f32x2_to_e4m3x2(x[d0], x[d0 + 1]);
+            const uint32_t c23 = f32x2_to_e4m3x2(x[d0 + 2], x[d0 + 3]);
+            q8[term][t][h] = c01 | (c23 << 16);
+            uint32_t f01, f23;  // the terms' exact values back, for the next residual
+            e4m3x4_to_f16x4(q8[term][t][h], f01, f23);
+            const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&f01));
+            const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&f23));
+            x[d0] -= v01.x;
+            x[d0 + 1] -= v01.y;
+            x[d0 + 2] -= v23.x;
+            x[d0 + 3] -= v23.y;
+          }
+        }
+      }
+      // rows 2cq and 2cq + 1 of the accumulator are rows gq = 2cq, 2cq + 1 of lanes 8cq, 8cq + 4
+      row_scale[0] = __shfl_sync(0xffffffffu, down, 8 * cq);
+      row_scale[1] = __shfl_sync(0xffffffffu, down, 8 * cq + 4);
     }
   }
+
+  // score scale of rows 2cq and 2cq + 1 (with the fp8 rows' 2^-c), and in log2 units
+  const float srow[2] = {scale * row_scale[0], scale * row_scale[1]};
+  const float srow2[2] = {srow[0] * kLog2e, srow[1] * kLog2e};
 
   float slope[2] = {0.f, 0.f};
   if constexpr (FEAT) {
@@ -341,25 +411,34 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
       // row 2cq + (e & 1)
       float st[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (C::kPermD) {
-        // Lane (gq, cq) reads bytes [cq D/4, (cq + 1) D/4) of K rows gq and gq + 8: word q
-        // of its 16-byte chunk u holds d = cq D/4 + 4 kk + {0..3} of slice kk = 4u + q, the A
-        // operand pairs (2cq, 2cq+1) and (2cq+8, 2cq+9) of that slice.
+        // Lane (gq, cq) reads bytes [cq D/4, (cq + 1) D/4) of K rows gq and gq + 8: words
+        // 2tt and 2tt + 1 of its 16-byte chunk u are the A registers (rows gq | gq + 8) of
+        // k-step t = 2u + tt.  One accumulator per Q term keeps the MMA chains short.
+        float sx[kQT][4];
+#pragma unroll
+        for (int term = 0; term < kQT; ++term)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sx[term][e] = 0.f;
 #pragma unroll
         for (int u = 0; u < D / 64; ++u) {
           const uint4 k0 = *reinterpret_cast<const uint4*>(
               kst + C::raw_byte(16 * ch + gq, cq * (D / 4) + 16 * u));
           const uint4 k8 = *reinterpret_cast<const uint4*>(
               kst + C::raw_byte(16 * ch + gq + 8, cq * (D / 4) + 16 * u));
-          const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
-          const uint32_t w8[4] = {k8.x, k8.y, k8.z, k8.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t a[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(w0[q])),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w8[q])),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w0[q] >> 16)),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w8[q] >> 16))};
-            mma_16816<true>(st, a, qt[4 * u + q][0], qt[4 * u + q][1]);
+          for (int tt = 0; tt < 2; ++tt) {
+            const uint32_t a[4] = {tt ? k0.z : k0.x, tt ? k8.z : k8.x, tt ? k0.w : k0.y,
+                                   tt ? k8.w : k8.y};
+#pragma unroll
+            for (int term = 0; term < kQT; ++term)
+              mma_16832_e4m3(sx[term], a, q8[term][2 * u + tt][0], q8[term][2 * u + tt][1]);
           }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          st[e] = sx[0][e];
+#pragma unroll
+          for (int term = 1; term < kQT; ++term) st[e] += sx[term][e];
         }
       } else {
         // A fragments of the swizzled K rows: matrices (keys 0-7 | 8-15) x (d 0-7 | 8-15)
@@ -392,7 +471,7 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
         const int j = kc0 + gq + 8 * (e >> 1);
         float x;
         if constexpr (FEAT) {
-          x = st[e] * scale;
+          x = st[e] * srow[rr];
           if (p.softcap > 0.f) x = p.softcap * fast_tanh(x * inv_softcap);
           x += slope[rr] * static_cast<float>(j - ctx);
           if (p.qq_bias != nullptr && rv[rr] && j >= ctx && j <= rpos[rr] &&
@@ -400,7 +479,7 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
             x += __ldg(p.qq_bias + static_cast<size_t>(ri[rr]) * p.qq_stride + (j - ctx));
           x *= kLog2e;
         } else {
-          x = st[e] * scale_log2;
+          x = st[e] * srow2[rr];
         }
         if (need_mask) {
           const bool ok = rv[rr] && j >= rlo[rr] && j <= rpos[rr] && j < ke;
@@ -508,10 +587,9 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t w0 = h ? hi0 : lo0, w8 = h ? hi8 : lo8;
-            uint32_t a[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(w0)),
-                             e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
-                             e4m3x2_to_f16x2(static_cast<uint16_t>(w8)),
-                             e4m3x2_to_f16x2(static_cast<uint16_t>(w8 >> 16))};
+            uint32_t a[4];
+            e4m3x4_to_f16x4(w0, a[0], a[1]);
+            e4m3x4_to_f16x4(w8, a[2], a[3]);
             if (tail) {
               a[0] &= m01;
               a[1] &= m01;
@@ -733,11 +811,11 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
   cluster_sync();  // no CTA leaves while the cluster still reads its shared memory
 }
 
-template <int D, int KV, bool FEAT>
+template <int D, int KV, bool FEAT, int QT>
 cudaError_t launch_decode_t(const TileParams& tp, dim3 grid, int cluster_y, int cluster_z,
                             cudaStream_t stream) {
   using C = DecCfg<D, KV>;
-  auto kern = ua_decode_kernel<D, KV, FEAT>;
+  auto kern = ua_decode_kernel<D, KV, FEAT, QT>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -757,13 +835,15 @@ cudaError_t launch_decode_t(const TileParams& tp, dim3 grid, int cluster_y, int 
 template <int D>
 cudaError_t launch_decode_dispatch(const TileParams& tp, dim3 grid, int kv, bool feat,
                                    int cluster_y, int cluster_z, cudaStream_t s) {
-#define UA_DEC_CASE(KVV)                                                                  \
-  if (kv == KVV)                                                                          \
-    return feat ? launch_decode_t<D, KVV, true>(tp, grid, cluster_y, cluster_z, s)        \
-                : launch_decode_t<D, KVV, false>(tp, grid, cluster_y, cluster_z, s);
-  UA_DEC_CASE(KV_F16)
-  UA_DEC_CASE(KV_BF16)
-  UA_DEC_CASE(KV_E4M3)
+#define UA_DEC_CASE(KVV, QT)                                                              \
+  return feat ? launch_decode_t<D, KVV, true, QT>(tp, grid, cluster_y, cluster_z, s)      \
+              : launch_decode_t<D, KVV, false, QT>(tp, grid, cluster_y, cluster_z, s);
+  if (kv == KV_F16) UA_DEC_CASE(KV_F16, 1)
+  if (kv == KV_BF16) UA_DEC_CASE(KV_BF16, 1)
+  if (kv == KV_E4M3) {
+    if (tp.p.q_dtype == UA_DT_BF16) UA_DEC_CASE(KV_E4M3, 2)
+    UA_DEC_CASE(KV_E4M3, 3)
+  }
 #undef UA_DEC_CASE
   return cudaErrorInvalidValue;
 }
@@ -774,7 +854,7 @@ cudaError_t launch_decode_dispatch(const TileParams& tp, dim3 grid, int kv, bool
 template <int D, int KV>
 int decode_cluster_capacity_t(int cluster_y, int cluster_z) {
   using C = DecCfg<D, KV>;
-  auto kern = ua_decode_kernel<D, KV, false>;
+  auto kern = ua_decode_kernel<D, KV, false, KV == KV_E4M3 ? 2 : 1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
           cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)

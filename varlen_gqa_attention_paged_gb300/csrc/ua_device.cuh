@@ -211,6 +211,19 @@ __device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t 
   }
 }
 
+// D (16 x 8, fp32) += A (16 x 32, e4m3, row-major) * B (32 x 8, e4m3, column-major).
+// Fragments (lane = 4 gq + cq): a0 = A[gq][4cq..4cq+3], a1 = A[gq+8][4cq..], a2 =
+// A[gq][16+4cq..], a3 = A[gq+8][16+4cq..] (four codes a register, lowest k in the low
+// byte); b0 = B[4cq..4cq+3][gq], b1 = B[16+4cq..][gq]; the accumulator as in m16n8k16.
+__device__ __forceinline__ void mma_16832_e4m3(float* c, const uint32_t* a, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -406,6 +419,23 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// The four e4m3fn codes of a word -> two f16x2 words, exactly: `lo` holds bytes 0 and 1,
+// `hi` bytes 2 and 3 (one conversion per 16-bit half of the word).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Two floats -> two e4m3fn codes (round to nearest even, saturating at +-448), `lo` in the
+// low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 // Two e4m3fn codes (low byte first) -> two f16 values, exactly (every e4m3 value is an
 // f16 normal or zero; NaN stays NaN).
