@@ -53,7 +53,7 @@ def peaks():
 # only while these are unchanged).
 KERNEL_SOURCES = {
     "ua_attn_tile_kernel": ["ua_tile.cuh", "ua_tile_d*.cu", "ua_device.cuh", "ua_internal.h"],
-    "ua_decode_kernel": ["ua_decode.cuh", "ua_decode_d*.cu", "ua_tile.cuh", "ua_device.cuh",
+    "ua_decode_kernel": ["ua_decode.cuh", "ua_decode_*.cu", "ua_tile.cuh", "ua_device.cuh",
                          "ua_internal.h"],
     "ua_prefill_tm_kernel": ["ua_prefill_tm.cuh", "ua_prefill.cuh", "ua_prefill_d64.cu",
                              "ua_prefill_d128.cu", "ua_device.cuh", "ua_internal.h"],
@@ -76,7 +76,7 @@ def kernel_name(plan, head_dim):
     """The attention kernel a plan launches."""
     if plan["kernel"] in (8, 16):
         return "ua_prefill_tm_kernel" if head_dim <= 128 else "ua_prefill_wide_kernel"
-    if plan["kernel"] == 2:
+    if plan["kernel"] in (2, 32):
         return "ua_decode_kernel"
     return "ua_attn_tile_kernel"
 
@@ -389,19 +389,21 @@ def run_ours(args):
     e2e_steps = max(10, min(args.steps, 500))
     h2d = total
     d2h = out_host.numel() * out_host.element_size()
+    # the public prepared call: sizes and options marshalled once, per-step tensors passed
+    # at every call
+    prep = ua.prepare(dq, call.d["k_cache"], call.d["v_cache"], dcu, dsl, dbt,
+                      max_seqlen_q=inp.max_seqlen_q, max_seqlen_k=inp.max_seqlen_k,
+                      scale=inp.scale, softcap=inp.softcap, window_left=inp.window_left,
+                      alibi_slopes=call.d["alibi_slopes"], qq_bias=call.d["qq_bias"],
+                      sinks=call.d["sinks"], kv_scale=call.kv_scale, k_scale_tok=call.tok[0],
+                      v_scale_tok=call.tok[1], out=call.out, stream=stream)
     with torch.cuda.stream(stream):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(e2e_steps):
             dstage.copy_(stages[i % len(stages)], non_blocking=True)
-            ua.unified_attention(dq, call.d["k_cache"], call.d["v_cache"], dcu, dsl, dbt,
-                                 max_seqlen_q=inp.max_seqlen_q, max_seqlen_k=inp.max_seqlen_k,
-                                 scale=inp.scale, softcap=inp.softcap,
-                                 window_left=inp.window_left, alibi_slopes=call.d["alibi_slopes"],
-                                 qq_bias=call.d["qq_bias"], sinks=call.d["sinks"],
-                                 kv_scale=call.kv_scale, k_scale_tok=call.tok[0],
-                                 v_scale_tok=call.tok[1], out=call.out, stream=stream)
+            prep(q=dq, cu_seqlens_q=dcu, seq_lens_k=dsl, block_table=dbt, out=call.out)
             out_host.copy_(call.out, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
@@ -480,9 +482,10 @@ def run_ours(args):
         "e2e": {"value": round(world * tokens_per_step * e2e_steps / (e2e_ms * 1e-3), 1),
                 "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
-                "note": "public Python API per step: one pinned H2D of q + cu_seqlens_q + "
-                        "seq_lens_k + block table (staged together), the call, D2H of out; "
-                        "the KV cache stays resident"},
+                "note": "public Python API per step (the prepared call of "
+                        "varlen_gqa_attention_paged_gb300.prepare, given the step's tensors): "
+                        "one pinned H2D of q + cu_seqlens_q + seq_lens_k + block table (staged "
+                        "together), the call, D2H of out; the KV cache stays resident"},
         "gpu_launches": call.launches_per_call * args.steps,
         "clocks": clocks,
         "workloads": extra,

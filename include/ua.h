@@ -43,7 +43,11 @@
  * Conventions: every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  * legacy default stream) and never synchronises; the library keeps no pointer to
  * caller memory after the call returns.  Errors are returned as ua_status_t and no
- * C++ exception crosses the ABI.  Block ids outside [0, num_blocks) are not read:
+ * C++ exception crosses the ABI.  Per device, the library keeps what it looks up once
+ * (the SM count, the device address of its status word, recently encoded tensor maps of
+ * the caller's buffers, keyed by address and layout); none of it survives cudaDeviceReset,
+ * after which the library must not be called on that device again.
+ * Block ids outside [0, num_blocks) are not read:
  * the kernel treats the key as zero and raises UA_ERR_DEVICE_CHECK in the device
  * status word (see ua_device_status).
  */
@@ -131,7 +135,9 @@ typedef struct {
                           G heads (16-bit caches, or fp8 at head_dim <= 128: codes dequantised
                           to f16 in shared memory as in RocKE "fp8 KV cache", a bf16 q
                           taken as f16); 16: the same
-                          kernel with two such tiles of consecutive tokens per CTA */
+                          kernel with two such tiles of consecutive tokens per CTA; 32: the
+                          key-major decode tile of code 2 with eight consumer warps (128-key
+                          stages, one CTA per SM), for decode grids of at most one CTA per SM */
   int32_t block_m;     /* (query token x head) rows per q-block */
   int32_t n_part;      /* key-range partitions (1 on the 2D path) */
   int32_t grid_x;      /* q-block slots: num_seqs when slot_per_seq, else

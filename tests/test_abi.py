@@ -177,6 +177,11 @@ def test_dispatcher_decode_kernels():
     assert _plan(max_seqlen_q=3)["kernel"] == 1
     assert _plan(head_dim=256)["kernel"] == 1
     assert _plan(block_size=13)["kernel"] == 1
+    # a decode grid of at most one CTA per SM: the decode tile with eight consumer warps
+    p = _plan(num_seqs=4, total_q=4, max_seqlen_k=4096, num_q_heads=16, num_kv_heads=2,
+              window_left=-1, kv_dtype=_lib.UA_DT_F16)
+    assert p["kernel"] == 32 and p["grid_x"] * p["grid_y"] * p["grid_z"] <= 152
+    assert p["cluster_z"] == p["n_part"] and p["workspace_bytes"] == 0
 
 
 def test_dispatcher_prefill_kernels():

@@ -16,8 +16,8 @@ from . import _lib
 from ._lib import (UA_BACKEND_2D, UA_BACKEND_AUTO, UA_BACKEND_SPLIT, UA_DT_BF16, UA_DT_F8E4M3,
                    UA_DT_F16, UA_DT_F32, UA_PATH_2D, UA_PATH_SPLIT)
 
-__all__ = ["unified_attention", "plan", "device_status", "device_status_reset", "UaError",
-           "BACKENDS", "library_path"]
+__all__ = ["unified_attention", "prepare", "PreparedAttention", "plan", "device_status",
+           "device_status_reset", "UaError", "BACKENDS", "library_path"]
 
 BACKENDS = {"auto": UA_BACKEND_AUTO, "2d": UA_BACKEND_2D, "split": UA_BACKEND_SPLIT}
 _DTYPES = {torch.float16: UA_DT_F16, torch.bfloat16: UA_DT_BF16,
@@ -129,6 +129,91 @@ def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table
     if rc != 0:
         raise UaError(rc, "ua_unified_attention")
     return out
+
+
+class PreparedAttention:
+    """``unified_attention`` with its sizes and options marshalled once, for a loop that
+    calls it again and again with the same shapes (a decode loop, a captured step).
+
+    Built by :func:`prepare`.  Calling it passes new per-step tensors -- ``q``,
+    ``cu_seqlens_q``, ``seq_lens_k``, ``block_table``, ``out`` -- each of the prepared one's
+    shape, dtype and device (checked); any left out keeps the prepared tensor.  The caches,
+    the score features, the scales and the host sizes (``max_seqlen_q``/``max_seqlen_k``)
+    stay as prepared.  Returns ``out``.
+    """
+
+    _STEP = ("q", "cu_seqlens_q", "seq_lens_k", "block_table", "out")
+    _POS = {"q": 0, "out": 3, "cu_seqlens_q": 4, "seq_lens_k": 5, "block_table": 6}
+
+    def __init__(self, lib, args, shape, tensors, stream):
+        self._lib = lib
+        self._args = args
+        self._shape = shape
+        self._meta = {n: (tuple(t.shape), t.dtype, t.device) for n, t in tensors.items()}
+        self._keep = dict(tensors)
+        self._stream = stream
+        self.out = tensors["out"]
+
+    def __call__(self, q=None, cu_seqlens_q=None, seq_lens_k=None, block_table=None, out=None,
+                 stream=None):
+        args = self._args
+        for name, t in (("q", q), ("cu_seqlens_q", cu_seqlens_q), ("seq_lens_k", seq_lens_k),
+                        ("block_table", block_table), ("out", out)):
+            if t is None:
+                continue
+            if (tuple(t.shape), t.dtype, t.device) != self._meta[name] or not t.is_contiguous():
+                raise ValueError(f"{name}: shape, dtype, device or layout differs from the "
+                                 "prepared call")
+            args[self._POS[name]] = ctypes.c_void_p(t.data_ptr())
+            self._keep[name] = t
+        if stream is not None:
+            args[-2] = ctypes.c_void_p(stream.cuda_stream)
+        rc = self._lib.ua_unified_attention(*args)
+        if rc != 0:
+            raise UaError(rc, "ua_unified_attention")
+        return self._keep["out"]
+
+
+def prepare(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *, max_seqlen_q: int,
+            max_seqlen_k: int, scale: float | None = None, softcap: float = 0.0,
+            window_left: int = -1, alibi_slopes=None, qq_bias=None, sinks=None, kv_scale=None,
+            k_scale_tok=None, v_scale_tok=None, out=None, out_dtype=None, backend: str = "auto",
+            num_splits: int = 0, workspace=None, stream=None) -> PreparedAttention:
+    """Validate and marshal a ``unified_attention`` call once (same arguments); the
+    returned :class:`PreparedAttention` makes the call with new per-step tensors."""
+    lib = _lib.load()
+    total_q, hq, d = q.shape
+    num_blocks, block_size, hkv, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape:
+        raise ValueError("q, k_cache and v_cache disagree on shape")
+    if qq_bias is not None and qq_bias.shape[0] < max_seqlen_q:
+        raise ValueError("qq_bias needs at least max_seqlen_q rows")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens_k", seq_lens_k),
+                    ("block_table", block_table)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    if not (q.is_cuda and k_cache.is_cuda and v_cache.is_cuda):
+        raise ValueError("q, k_cache and v_cache must be CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sh = _shape(q, k_cache, block_table, cu_seqlens_q, max_seqlen_q, max_seqlen_k, qq_bias,
+                _dtype_code(out), num_splits, workspace, None, k_scale_tok, v_scale_tok)
+    args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(cu_seqlens_q),
+            _ptr(seq_lens_k), _ptr(block_table), block_size, hq, hkv, d, float(scale),
+            float(softcap or 0.0), int(window_left if window_left is not None else -1),
+            _ptr(alibi_slopes), _ptr(qq_bias), _ptr(sinks), _dtype_code(k_cache), _ptr(kv_scale),
+            BACKENDS[backend], ctypes.c_void_p(stream.cuda_stream), ctypes.byref(sh)]
+    tensors = {"q": q, "cu_seqlens_q": cu_seqlens_q, "seq_lens_k": seq_lens_k,
+               "block_table": block_table, "out": out}
+    prep = PreparedAttention(lib, args, sh, tensors, stream)
+    # the caches, score features and scales the prepared call points at stay alive with it
+    prep._static = (k_cache, v_cache, alibi_slopes, qq_bias, sinks, kv_scale, k_scale_tok,
+                    v_scale_tok, workspace)
+    return prep
 
 
 def plan(*, num_seqs, total_q, max_seqlen_q, max_seqlen_k, block_size, num_q_heads,

@@ -58,10 +58,55 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Recently encoded tensor maps, keyed by everything that goes into one (base address,
+// element type, extents, box): a steady stream of calls on the same cache and query buffers
+// reuses its maps instead of encoding them again.  Small, round-robin replacement.
+struct MapKey {
+  const void* base;
+  int kind, dtype, d, heads, rows, box_y, box_z;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && kind == o.kind && dtype == o.dtype && d == o.d && heads == o.heads &&
+           rows == o.rows && box_y == o.box_y && box_z == o.box_z;
+  }
+};
+
+class MapCache {
+ public:
+  bool find(const MapKey& k, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(mu_);
+    for (int i = 0; i < used_; ++i)
+      if (keys_[i] == k) {
+        *out = maps_[i];
+        return true;
+      }
+    return false;
+  }
+  void put(const MapKey& k, const CUtensorMap& m) {
+    std::lock_guard<std::mutex> lock(mu_);
+    const int i = used_ < kSize ? used_++ : (next_++ % kSize);
+    keys_[i] = k;
+    maps_[i] = m;
+  }
+
+ private:
+  static constexpr int kSize = 32;
+  std::mutex mu_;
+  MapKey keys_[kSize];
+  CUtensorMap maps_[kSize];
+  int used_ = 0, next_ = 0;
+};
+
+MapCache& map_cache() {
+  static MapCache* c = new MapCache();  // never destroyed
+  return *c;
+}
+
 // q [total_q][H_q][D] as a 3-D TMA tensor; one box is the 64-element column block `x` of
 // G heads x tq tokens, written as G*tq rows of 128 bytes (128-byte swizzle).
 bool encode_q_map(CUtensorMap* map, const void* q, int q_dtype, int total_q, int hq, int d,
                   int group, int tq) {
+  const MapKey key{q, 0, q_dtype, d, hq, total_q, group, tq};
+  if (map_cache().find(key, map)) return true;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hq),
@@ -75,7 +120,9 @@ bool encode_q_map(CUtensorMap* map, const void* q, int q_dtype, int total_q, int
           3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  map_cache().put(key, *map);
+  return true;
 }
 
 // A paged cache [num_blocks * block_size][H_kv][D] as a 3-D TMA tensor; one box is 16
@@ -83,6 +130,8 @@ bool encode_q_map(CUtensorMap* map, const void* q, int q_dtype, int total_q, int
 // unswizzled).  Rows past the tensor read as zero.
 bool encode_cache_map(CUtensorMap* map, const void* base, int kv_dtype, int num_blocks,
                       int block_size, int hkv, int d) {
+  const MapKey key{base, 1, kv_dtype, d, hkv, num_blocks, block_size, 0};
+  if (map_cache().find(key, map)) return true;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const int esz = kv_dtype == UA_DT_F8E4M3 ? 1 : 2;
@@ -101,7 +150,28 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int kv_dtype, int num_
                          CU_TENSOR_MAP_INTERLEAVE_NONE,
                          cbw == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  map_cache().put(key, *map);
+  return true;
+}
+
+// Device address of the status word on the current device (looked up once per device; the
+// address does not survive cudaDeviceReset of that device).
+int status_word(unsigned int** out) {
+  static std::mutex mu;
+  static std::map<int, unsigned int*> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it == cache.end()) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess || ptr == nullptr)
+      return UA_ERR_CUDA;
+    it = cache.emplace(dev, static_cast<unsigned int*>(ptr)).first;
+  }
+  *out = it->second;
+  return UA_OK;
 }
 
 int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int kv_dtype,
@@ -217,13 +287,28 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
       const int c = cy * cz;
       if (c <= 1) break;
       long long cap = -1;
-      if (dec && query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, cy, cz);
+      if (dec && query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, false, cy, cz);
       if (cap < 0) cap = c <= 2 ? wave / c : (wave * 9 / 10) / c;
       if (slots * (hkv / cy) <= cap) break;
     }
   }
+  // A decode grid of at most one CTA per SM runs the eight-warp decode tile (128-key
+  // stages): twice the consumer warps on each CTA's key walk, half the pipeline stages,
+  // when its clusters (one CTA per SM) are all resident together.
+  bool wide = false;
+  if (dec && slots * hkv * n_part <= num_sms) {
+    int cy, cz;
+    cluster_shape(n_part, cy, cz);
+    wide = true;
+    if (cy * cz > 1) {
+      long long cap = -1;
+      if (query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, true, cy, cz);
+      if (cap < 0) cap = (static_cast<long long>(num_sms) * 9 / 10) / (cy * cz);
+      wide = slots * (hkv / cy) <= cap;
+    }
+  }
   pl->path = n_part > 1 ? UA_PATH_SPLIT : UA_PATH_2D;
-  pl->kernel = tc ? (nq == 2 ? ua::KERNEL_TC256 : ua::KERNEL_TC128) : wm;
+  pl->kernel = tc ? (nq == 2 ? ua::KERNEL_TC256 : ua::KERNEL_TC128) : wide ? ua::KERNEL_DEC8W : wm;
   pl->block_m = bm;
   pl->n_part = n_part;
   pl->grid_x = static_cast<int32_t>(slots);
@@ -357,8 +442,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   p.out_dtype = sh->out_dtype;
   p.scale = scale;
   p.softcap = softcap > 0.f ? softcap : 0.f;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
-    return UA_ERR_CUDA;
+  if ((rc = status_word(&p.status)) != UA_OK) return rc;
 
   const int kv = kv_dtype == UA_DT_F16 ? ua::KV_F16 : kv_dtype == UA_DT_BF16 ? ua::KV_BF16 : ua::KV_E4M3;
   const bool feat = softcap > 0.f || alibi != nullptr || qq_bias != nullptr;
@@ -386,14 +470,16 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   if (tma)
     tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
           encode_cache_map(&tp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d);
-  if (pl.kernel == ua::KERNEL_DEC8 && !tma) {
+  const bool dec_kernel = pl.kernel == ua::KERNEL_DEC8 || pl.kernel == ua::KERNEL_DEC8W;
+  if (dec_kernel && !tma) {
     make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, false, false,
               true, &pl);
     p.n_part = pl.n_part;
   }
   // per-token fp8 scales: the decode tile reads them (decode batches, head_dim <= 128,
   // 16 | block_size); other shapes have no kernel for them
-  if (tok_scales && pl.kernel != ua::KERNEL_DEC8) return UA_ERR_UNSUPPORTED;
+  if (tok_scales && pl.kernel != ua::KERNEL_DEC8 && pl.kernel != ua::KERNEL_DEC8W)
+    return UA_ERR_UNSUPPORTED;
   p.cluster_merge = pl.cluster_z > 1 ? 1 : 0;
   if (pl.n_part > 1 && !p.cluster_merge) {
     void* ws = sh->workspace;
@@ -421,8 +507,11 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
       default: err = ua::launch_prefill_d256(pp, grid, kv, feat, nq, st); break;
     }
   } else if (pl.kernel == ua::KERNEL_DEC8) {
-    err = d == 64 ? ua::launch_decode_d64(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st)
-                  : ua::launch_decode_d128(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st);
+    err = d == 64 ? ua::launch_decode_w4_d64(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st)
+                  : ua::launch_decode_w4_d128(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st);
+  } else if (pl.kernel == ua::KERNEL_DEC8W) {
+    err = d == 64 ? ua::launch_decode_w8_d64(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st)
+                  : ua::launch_decode_w8_d128(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st);
   } else switch (d) {
     case 64: err = ua::launch_tile_d64(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, pl.cluster_z, st); break;
     case 128: err = ua::launch_tile_d128(tp, grid, pl.kernel, kv, feat, tma, pl.cluster_y, pl.cluster_z, st); break;

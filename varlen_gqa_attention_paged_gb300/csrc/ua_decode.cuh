@@ -24,12 +24,15 @@
 
 namespace ua {
 
-template <int D, int KV>
+// W consumer warps (4, or 8 for grids of at most one CTA per SM), each taking 16 keys of
+// every stage.
+template <int D, int KV, int W = 4>
 struct DecCfg {
-  static constexpr int kConsumerWarps = 4;
+  static constexpr int kConsumerWarps = W;
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);
   static constexpr int kRows = 8;                  // rows of a q-block (the MMA's N)
-  static constexpr int kT = 64;                    // keys per pipeline stage (4 pages of 16)
+  static constexpr int kT = 16 * W;                // keys per pipeline stage (W pages of 16)
+  static constexpr int kKPL = kT / 32;             // keys whose scales one producer lane stages
   static constexpr int kEsz = KvTraits<KV>::kEsz;
   static constexpr int kRowBytes = D * kEsz;       // one K or V row in the cache
   static constexpr bool kSwz = kRowBytes >= 128;   // 128-byte swizzled column blocks
@@ -43,8 +46,9 @@ struct DecCfg {
   // [4][kMT][32] float4; then the CTA's partial rows [8][D], maxima [8] and sums [8]
   static constexpr int kMergeBytes = kConsumerWarps * (2 * kRows + kMT * 32 * 4) * 4;
   static constexpr int kPartBytes = kRows * (D + 2) * 4;
-  // three CTAs per SM: at most ~72 KB of shared memory each
-  static constexpr int kBudget = 72 * 1024;
+  // four consumer warps: three CTAs per SM, at most ~72 KB of shared memory each; eight:
+  // one CTA per SM
+  static constexpr int kBudget = W == 4 ? 72 * 1024 : 200 * 1024;
   static constexpr int kStagesFit = kBudget / kStageBytes;
   static constexpr int kStages = kStagesFit < 2 ? 2 : (kStagesFit > 6 ? 6 : kStagesFit);
   static constexpr int kPipeRaw = (kStages * kStageBytes > kMergeBytes + kPartBytes)
@@ -54,7 +58,8 @@ struct DecCfg {
   // fp8 per-token scales of a stage's keys, K then V, behind the barriers
   static constexpr int kScaleBytes = kPermD ? kStages * 2 * kT * 4 : 0;
   static constexpr int kSmemBytes = 1024 + kPipeBytes + 2 * kStages * 8 + kScaleBytes;
-  static constexpr int kMinBlocks = (3 * (kSmemBytes + 1024) <= 228 * 1024) ? 3 : 2;
+  static constexpr int kMinBlocks = W != 4 ? 1 : (3 * (kSmemBytes + 1024) <= 228 * 1024) ? 3 : 2;
+  static_assert(W == 4 || W == 8, "four or eight consumer warps");
   static_assert(D <= 128, "the key-major decode tile covers head_dim <= 128");
   static_assert(kRowBytes % kCBW == 0 && kCBW % 16 == 0, "rows are whole column blocks");
 
@@ -72,10 +77,11 @@ struct DecCfg {
 };
 
 // QT: e4m3 terms of Q for fp8 caches (2 for a bf16 q, 3 for an f16 q); unused otherwise.
-template <int D, int KV, bool FEAT, int QT>
-__global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
+// W: consumer warps of a CTA.
+template <int D, int KV, bool FEAT, int QT, int W>
+__global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>::kMinBlocks))
     ua_decode_kernel(const __grid_constant__ TileParams tp) {
-  using C = DecCfg<D, KV>;
+  using C = DecCfg<D, KV, W>;
   constexpr int T = C::kT;
   constexpr int S = C::kStages;
   constexpr int NR = C::kRows;
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
 
   if (warp == C::kConsumerWarps) {
     // ======================================================== producer warp
-    // lane j < 4 owns page slice j (keys key0 + 16j .. +15) of every tile: one TMA box of
+    // lane j < W owns page slice j (keys key0 + 16j .. +15) of every tile: one TMA box of
     // 16 cache rows per column block, K and V; rows with no key read the zero-filled row
     // coordinate past the cache.
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
@@ -158,20 +164,21 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
       }
       return blk * bs + key % bs;
     };
-    // Per-token scales of this lane's keys 2 lane and 2 lane + 1 of tile t (one page; 0 past
+    // Per-token scales of this lane's kKPL keys kKPL lane .. of tile t (one page; 0 past
     // the walk): the page's block id is loaded two tiles ahead, the scales one tile ahead.
+    constexpr int KPL = C::kKPL;
     auto scale_blk = [&](int t) -> int {
-      const int key = ks + t * T + 2 * lane;
+      const int key = ks + t * T + KPL * lane;
       if (t >= ntiles || key >= ke) return -1;
       const int col = key / bs;
       const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
       return static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks) ? blk : -1;
     };
-    auto load_scales = [&](int t, int blk, float (&kv)[2][2]) {
+    auto load_scales = [&](int t, int blk, float (&kv)[KPL][2]) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
+      for (int e = 0; e < KPL; ++e) {
         kv[e][0] = kv[e][1] = 0.f;
-        const int key = ks + t * T + 2 * lane + e;
+        const int key = ks + t * T + KPL * lane + e;
         if (blk < 0 || key >= ke) continue;
         const long long slot = key % bs;
         kv[e][0] = __ldg(p.k_scale_tok + blk * p.k_scale_stride[0] + slot * p.k_scale_stride[1] +
@@ -180,7 +187,9 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
                          g * p.v_scale_stride[2]);
       }
     };
-    float sc_next[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    float sc_next[KPL][2];
+#pragma unroll
+    for (int e = 0; e < KPL; ++e) sc_next[e][0] = sc_next[e][1] = 0.f;
     int blk_next = -1;
     if (tok) {
       if (ntiles > 0) load_scales(0, scale_blk(0), sc_next);
@@ -192,9 +201,9 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
       const int s = t % S;
       const int row = row_next;
       if (t + 1 < ntiles) row_next = page_row(t + 1);  // block-table lookups one tile ahead
-      float sc_cur[2][2];
+      float sc_cur[KPL][2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
+      for (int e = 0; e < KPL; ++e) {
         sc_cur[e][0] = sc_next[e][0];
         sc_cur[e][1] = sc_next[e][1];
       }
@@ -219,10 +228,11 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
         }
       }
       if (tok) {  // after the copies are on their way; released to the consumers by lane 0
-        sks[s * T + 2 * lane] = sc_cur[0][0];
-        sks[s * T + 2 * lane + 1] = sc_cur[1][0];
-        svs[s * T + 2 * lane] = sc_cur[0][1];
-        svs[s * T + 2 * lane + 1] = sc_cur[1][1];
+#pragma unroll
+        for (int e = 0; e < KPL; ++e) {
+          sks[s * T + KPL * lane + e] = sc_cur[e][0];
+          svs[s * T + KPL * lane + e] = sc_cur[e][1];
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[s]);
       }
@@ -645,9 +655,9 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
   // ---- the four warps' states of the same rows: rescale to the rows' max (exchanged
   // through shared memory), warp 0 adds the others' partial outputs (read in the MMA
   // fragment layout) and leaves the CTA's partial rows in shared memory.
-  float* const sm_m = reinterpret_cast<float*>(pipe);                  // [4][8]
-  float* const sm_l = sm_m + C::kConsumerWarps * NR;                   // [4][8]
-  float4* const sm_o = reinterpret_cast<float4*>(sm_l + C::kConsumerWarps * NR);  // [4][kMT][32]
+  float* const sm_m = reinterpret_cast<float*>(pipe);                  // [W][8]
+  float* const sm_l = sm_m + C::kConsumerWarps * NR;                   // [W][8]
+  float4* const sm_o = reinterpret_cast<float4*>(sm_l + C::kConsumerWarps * NR);  // [W][kMT][32]
   float* const partial = reinterpret_cast<float*>(pipe + C::kMergeBytes);  // [8][D], m[8], l[8]
   if (gq == 0) {
     sm_m[warp * NR + 2 * cq] = m_run[0];
@@ -811,11 +821,11 @@ __global__ void __launch_bounds__(160, (DecCfg<D, KV>::kMinBlocks))
   cluster_sync();  // no CTA leaves while the cluster still reads its shared memory
 }
 
-template <int D, int KV, bool FEAT, int QT>
+template <int D, int KV, bool FEAT, int QT, int W>
 cudaError_t launch_decode_t(const TileParams& tp, dim3 grid, int cluster_y, int cluster_z,
                             cudaStream_t stream) {
-  using C = DecCfg<D, KV>;
-  auto kern = ua_decode_kernel<D, KV, FEAT, QT>;
+  using C = DecCfg<D, KV, W>;
+  auto kern = ua_decode_kernel<D, KV, FEAT, QT, W>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -832,12 +842,12 @@ cudaError_t launch_decode_t(const TileParams& tp, dim3 grid, int cluster_y, int 
                             cluster_z, tp);
 }
 
-template <int D>
-cudaError_t launch_decode_dispatch(const TileParams& tp, dim3 grid, int kv, bool feat,
-                                   int cluster_y, int cluster_z, cudaStream_t s) {
-#define UA_DEC_CASE(KVV, QT)                                                              \
-  return feat ? launch_decode_t<D, KVV, true, QT>(tp, grid, cluster_y, cluster_z, s)      \
-              : launch_decode_t<D, KVV, false, QT>(tp, grid, cluster_y, cluster_z, s);
+template <int D, int W>
+cudaError_t launch_decode_width(const TileParams& tp, dim3 grid, int kv, bool feat,
+                                int cluster_y, int cluster_z, cudaStream_t s) {
+#define UA_DEC_CASE(KVV, QT)                                                                 \
+  return feat ? launch_decode_t<D, KVV, true, QT, W>(tp, grid, cluster_y, cluster_z, s)      \
+              : launch_decode_t<D, KVV, false, QT, W>(tp, grid, cluster_y, cluster_z, s);
   if (kv == KV_F16) UA_DEC_CASE(KV_F16, 1)
   if (kv == KV_BF16) UA_DEC_CASE(KV_BF16, 1)
   if (kv == KV_E4M3) {
@@ -851,10 +861,10 @@ cudaError_t launch_decode_dispatch(const TileParams& tp, dim3 grid, int kv, bool
 // Clusters of cluster_y x cluster_z CTAs of the decode kernel that can be resident at
 // once (the hardware places a cluster's CTAs within one GPU processing cluster, so fewer
 // CTAs than the SMs' slots may run together); -1 when the query fails.
-template <int D, int KV>
+template <int D, int KV, int W>
 int decode_cluster_capacity_t(int cluster_y, int cluster_z) {
-  using C = DecCfg<D, KV>;
-  auto kern = ua_decode_kernel<D, KV, false, KV == KV_E4M3 ? 2 : 1>;
+  using C = DecCfg<D, KV, W>;
+  auto kern = ua_decode_kernel<D, KV, false, KV == KV_E4M3 ? 2 : 1, W>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
           cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
@@ -875,10 +885,10 @@ int decode_cluster_capacity_t(int cluster_y, int cluster_z) {
   return n;
 }
 
-template <int D>
+template <int D, int W>
 int decode_cluster_capacity_d(int kv, int cluster_y, int cluster_z) {
-  return kv == KV_E4M3 ? decode_cluster_capacity_t<D, KV_E4M3>(cluster_y, cluster_z)
-                       : decode_cluster_capacity_t<D, KV_BF16>(cluster_y, cluster_z);
+  return kv == KV_E4M3 ? decode_cluster_capacity_t<D, KV_E4M3, W>(cluster_y, cluster_z)
+                       : decode_cluster_capacity_t<D, KV_BF16, W>(cluster_y, cluster_z);
 }
 
 template <int D>

@@ -90,14 +90,23 @@ cudaError_t launch_tile_d128(const TileParams& tp, dim3 grid, int wm, int kv, bo
                              int cluster_y, int cluster_z, cudaStream_t s);
 cudaError_t launch_tile_d256(const TileParams& tp, dim3 grid, int wm, int kv, bool feat, bool tma,
                              int cluster_y, int cluster_z, cudaStream_t s);
-// key-major decode tile (head_dim 64, 128; TMA page boxes; at most 8 rows per kv-head)
-cudaError_t launch_decode_d64(const TileParams& tp, dim3 grid, int kv, bool feat, int cluster_y,
-                              int cluster_z, cudaStream_t s);
-cudaError_t launch_decode_d128(const TileParams& tp, dim3 grid, int kv, bool feat, int cluster_y,
-                               int cluster_z, cudaStream_t s);
+// key-major decode tile (head_dim 64, 128; TMA page boxes; at most 8 rows per kv-head), with
+// four consumer warps (64-key stages, three CTAs per SM) or eight (128-key stages, one CTA
+// per SM, for small grids)
+cudaError_t launch_decode_w4_d64(const TileParams& tp, dim3 grid, int kv, bool feat,
+                                 int cluster_y, int cluster_z, cudaStream_t s);
+cudaError_t launch_decode_w4_d128(const TileParams& tp, dim3 grid, int kv, bool feat,
+                                  int cluster_y, int cluster_z, cudaStream_t s);
+cudaError_t launch_decode_w8_d64(const TileParams& tp, dim3 grid, int kv, bool feat,
+                                 int cluster_y, int cluster_z, cudaStream_t s);
+cudaError_t launch_decode_w8_d128(const TileParams& tp, dim3 grid, int kv, bool feat,
+                                  int cluster_y, int cluster_z, cudaStream_t s);
+// resident CTAs per SM of the four-warp decode tile
 int decode_ctas_per_sm(int head_dim, int kv);
-// co-resident clusters of cluster_y x cluster_z decode CTAs on the current device (-1: unknown)
-int decode_cluster_capacity(int head_dim, int kv, int cluster_y, int cluster_z);
+// co-resident clusters of cluster_y x cluster_z decode CTAs (four or, wide, eight consumer
+// warps) on the current device (-1: unknown); cached per device
+int decode_cluster_capacity(int head_dim, int kv, bool wide, int cluster_y, int cluster_z);
+int decode_cluster_capacity_w8(int head_dim, int kv, int cluster_y, int cluster_z);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_prefill_d64(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
                                cudaStream_t s);
@@ -107,7 +116,8 @@ cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool
                                cudaStream_t s);
 
 // Plan kernel codes.
-enum : int { KERNEL_TILE16 = 1, KERNEL_DEC8 = 2, KERNEL_TILE64 = 4, KERNEL_TC128 = 8, KERNEL_TC256 = 16 };
+enum : int { KERNEL_TILE16 = 1, KERNEL_DEC8 = 2, KERNEL_TILE64 = 4, KERNEL_TC128 = 8, KERNEL_TC256 = 16,
+             KERNEL_DEC8W = 32 };
 
 // Resident CTAs per SM of the tile kernel variant for (head_dim, kv dtype, wm).
 int tile_ctas_per_sm(int head_dim, int kv, int wm);
