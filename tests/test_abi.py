@@ -193,9 +193,11 @@ def test_dispatcher_prefill_kernels():
         for d in (64, 128):
             p = _plan(kv_dtype=kv, head_dim=d, **prefill)
             assert p["kernel"] == 16 and p["block_m"] == 2 * 128, (kv, d)
-    # fp8 at head_dim 256: the 64-row tile kernel
-    assert _plan(kv_dtype=_lib.UA_DT_F8E4M3, head_dim=256, **prefill)["kernel"] == 4
+    # head_dim 256 (16-bit or fp8 caches): the tensor-memory kernel, one q tile a CTA
+    assert _plan(kv_dtype=_lib.UA_DT_F8E4M3, head_dim=256, **prefill)["kernel"] == 8
     assert _plan(kv_dtype=_lib.UA_DT_BF16, head_dim=256, **prefill)["kernel"] == 8
+    # pages not a multiple of 16: the 64-row tile kernel
+    assert _plan(kv_dtype=_lib.UA_DT_F8E4M3, block_size=13, **prefill)["kernel"] == 4
 
 
 def test_dispatcher_mixed_batch_splits_underfilled_long_walks():

@@ -96,8 +96,9 @@ def _tile_rows(inp, tokens_per_tile, tiles_per_seq=64):
 
 
 @pytest.mark.parametrize("spec,kernel", [(W.PREFILL_D128, 16), (W.PREFILL_D128_FP8, 16),
-                                         (W.PREFILL_D256, 8)],
-                         ids=["prefill_d128", "prefill_d128_fp8", "prefill_d256"])
+                                         (W.PREFILL_D256, 8), (W.PREFILL_D256_FP8, 8)],
+                         ids=["prefill_d128", "prefill_d128_fp8", "prefill_d256",
+                              "prefill_d256_fp8"])
 def test_long_prefill_sampled_rows(spec, kernel):
     """Full-size prefill in the bench's launch configuration: every head of the first and
     last token of 64 q tiles per sequence (over 15,000 rows) against the oracle, for the
@@ -217,6 +218,29 @@ SMALL = {
                                    num_q_heads=32, num_kv_heads=8, block_size=32,
                                    q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
                                    window=256),
+    # fp8 caches at head_dim 256 on the tensor-memory kernel: half tiles of codes staged and
+    # dequantised to f16 slots; odd and even tile counts, every score feature at G = 16
+    "pf_fp8_d256_window_sinks": dict(seqs=[(130, 390), (1, 129), (64, 64), (257, 900)],
+                                     num_q_heads=8, num_kv_heads=2, head_dim=256,
+                                     kv_dtype=torch.float8_e4m3fn, window=200, sinks=True),
+    "pf_fp8_d256_bf16q_g16_feat": dict(seqs=[(40, 500), (9, 9), (100, 300)], num_q_heads=16,
+                                       num_kv_heads=1, head_dim=256, block_size=64,
+                                       q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
+                                       softcap=30.0, alibi=True, qq_bias=True,
+                                       qq_bias_shape=(100, 112), sinks=True),
+    # per-token fp8 scales (V's with other strides) on the tensor-memory kernels: each key's
+    # row is dequantised times its own scale
+    "pf_fp8_tok_d128_window": dict(seqs=[(200, 500), (129, 129), (1, 300), (37, 45)],
+                                   num_q_heads=32, num_kv_heads=8, q_dtype=torch.bfloat16,
+                                   kv_dtype=torch.float8_e4m3fn, per_token_scales=True,
+                                   window=150, sinks=True),
+    "pf_fp8_tok_d64_feat": dict(seqs=[(300, 700), (1, 65), (130, 130)], num_q_heads=16,
+                                num_kv_heads=2, head_dim=64, block_size=32,
+                                kv_dtype=torch.float8_e4m3fn, per_token_scales=True,
+                                softcap=25.0, alibi=True, sinks=True),
+    "pf_fp8_tok_d256": dict(seqs=[(130, 390), (64, 64), (257, 600)], num_q_heads=8,
+                            num_kv_heads=2, head_dim=256, q_dtype=torch.bfloat16,
+                            kv_dtype=torch.float8_e4m3fn, per_token_scales=True, window=300),
     # head_dim 256: K and V stream as half tiles through one ring; odd and even tile counts
     "pf_f16_d256_ragged": dict(seqs=[(130, 390), (1, 129), (64, 64), (257, 900)],
                                num_q_heads=8, num_kv_heads=2, head_dim=256),
@@ -411,9 +435,17 @@ def test_cuda_graph_capture_and_replay(spec, kw):
         assert max_err(out, want) <= TOL[spec.kv_dtype], (spec.name, replica)
 
 
-def test_per_token_scales_outside_the_decode_tile_are_unsupported():
-    # prefill-shaped rows (more than 8 per kv-head): no kernel reads per-token scales
-    inp = W.make(_small(11, kv_dtype=torch.float8_e4m3fn, per_token_scales=True))
+def test_per_token_scales_on_the_tile_kernel_are_unsupported():
+    # 9 to 16 rows per kv-head (the 16-row tile kernel): no per-token scales there
+    inp = W.make(_small(11, seqs=[(2, 300), (1, 40)], num_q_heads=16, num_kv_heads=2,
+                        kv_dtype=torch.float8_e4m3fn, per_token_scales=True))
+    assert _plan(inp)["kernel"] == 1
+    with pytest.raises(ua.UaError) as e:
+        run(inp)
+    assert e.value.code == ua._lib.UA_ERR_UNSUPPORTED
+    # pages not a multiple of 16 (the 64-row tile kernel): neither
+    inp = W.make(_small(13, block_size=13, kv_dtype=torch.float8_e4m3fn, per_token_scales=True))
+    assert _plan(inp)["kernel"] == 4
     with pytest.raises(ua.UaError) as e:
         run(inp)
     assert e.value.code == ua._lib.UA_ERR_UNSUPPORTED

@@ -201,11 +201,11 @@ int check_sizes(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, in
 // Kernel: decode calls with at most 8 rows per kv-head, head_dim <= 128 and page-sized
 // TMA boxes take the key-major decode tile (keys on the MMA's M side, rows on N); other
 // decode-shaped calls (every sequence's rows fit 16) take the warp-MMA tile kernel with
-// 16-row q-blocks; other calls with 16 | block_size (fp16/bf16 caches, or fp8 at head_dim
-// <= 128) take the tensor-memory kernel with 128-row q tiles (floor(128 / G) tokens x G
-// heads), two tiles per CTA for head_dim <= 128 when that grid still fills the device; the
-// rest (fp8 caches at head_dim 256, other block sizes) take the tile kernel with 64-row
-// q-blocks.
+// 16-row q-blocks; other calls with 16 | block_size take the tensor-memory kernels with
+// 128-row q tiles (floor(128 / G) tokens x G heads; fp8 caches dequantised to f16 tiles in
+// shared memory), two tiles per CTA for head_dim <= 128 when that grid still fills the
+// device; the rest (block sizes not a multiple of 16) take the tile kernel with 64-row
+// q-blocks.  A decode grid of at most one CTA per SM takes the eight-warp decode tile.
 bool is_tc(int kernel) { return kernel == ua::KERNEL_TC128 || kernel == ua::KERNEL_TC256; }
 
 void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int window_left,
@@ -213,9 +213,7 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
                bool query_device, ua_plan_t* pl) {
   const int group = hq / hkv;
   const long long rows_max = static_cast<long long>(sh->max_seqlen_q) * group;
-  const bool tc = allow_tc && rows_max > 16 && group <= 128 && block_size % 16 == 0 &&
-                  (kv_dtype == UA_DT_F16 || kv_dtype == UA_DT_BF16 ||
-                   (kv_dtype == UA_DT_F8E4M3 && d <= 128));
+  const bool tc = allow_tc && rows_max > 16 && group <= 128 && block_size % 16 == 0;
   // decode with at most 8 rows per kv-head: the key-major decode tile (page boxes)
   const bool dec = allow_dec && !tc && rows_max <= 8 && d <= 128 && block_size % 16 == 0 &&
                    static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
@@ -478,7 +476,10 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   }
   // per-token fp8 scales: the decode tile reads them (decode batches, head_dim <= 128,
   // 16 | block_size); other shapes have no kernel for them
-  if (tok_scales && pl.kernel != ua::KERNEL_DEC8 && pl.kernel != ua::KERNEL_DEC8W)
+  // per-token fp8 scales: the decode tile and the tensor-memory kernels read them (the tile
+  // kernel, for 9 to 16 rows a kv-head or pages not a multiple of 16, does not)
+  if (tok_scales && pl.kernel != ua::KERNEL_DEC8 && pl.kernel != ua::KERNEL_DEC8W &&
+      !is_tc(pl.kernel))
     return UA_ERR_UNSUPPORTED;
   p.cluster_merge = pl.cluster_z > 1 ? 1 : 0;
   if (pl.n_part > 1 && !p.cluster_merge) {

@@ -50,7 +50,9 @@
 
 namespace ua {
 
-template <int D, int NQ, bool F8 = false>
+// SW: softmax warps per tensor-memory lane quarter of a q tile (1, or 2 splitting the key
+// columns of S and the columns of O between them).
+template <int D, int NQ, bool F8 = false, int SW = 1>
 struct PrefillTmCfg {
   static constexpr int kBM = 128;                        // MMA rows of one q tile
   static constexpr int kBN = 128;                        // keys per tile
@@ -63,16 +65,20 @@ struct PrefillTmCfg {
   static constexpr int kF8Tile = kBN * D;
   static constexpr int kF8Bytes = F8 ? 2 * kF8Tile : 0;
   static constexpr int kDeqWarps = F8 ? 4 : 0;
+  // SW > 1: the row maxima of each tile (two buffers) and the final row sums of the SW
+  // warps of a row, exchanged through shared memory
+  static constexpr int kXchBytes = SW > 1 ? NQ * SW * 3 * 128 * 4 : 0;
   // K and V ring depths: as many tiles as fit beside Q (K gets the odd one, at most 4 each)
   static constexpr int kSlots =
-      (227 * 1024 - 1024 - kBarBytes - NQ * kQBytes - kF8Bytes) / kTileBytes;
+      (227 * 1024 - 1024 - kBarBytes - NQ * kQBytes - kF8Bytes - kXchBytes) / kTileBytes;
   static constexpr int kRingK = (kSlots + 1) / 2 > 4 ? 4 : (kSlots + 1) / 2;
   static constexpr int kRingV = kSlots / 2 > 4 ? 4 : kSlots / 2;
   static constexpr int kSmemBytes =
-      1024 + NQ * kQBytes + (kRingK + kRingV) * kTileBytes + kF8Bytes + kBarBytes;
+      1024 + NQ * kQBytes + (kRingK + kRingV) * kTileBytes + kF8Bytes + kBarBytes + kXchBytes;
   static constexpr int kTmemStride = kBN + D;            // S/P, then O, of one q tile
   static constexpr int kTmemCols = 512;
-  static constexpr int kSoftmaxWarps = 4 * NQ;
+  static constexpr int kSoftmaxWarps = 4 * NQ * SW;
+  static_assert(SW == 1 || SW == 2, "one or two softmax warps per lane quarter");
   static constexpr int kThreads = 32 * kSoftmaxWarps + 96 + 32 * kDeqWarps;
   static_assert(D <= 128, "two 128-key K/V rings must fit");
   static_assert(NQ * kTmemStride <= kTmemCols, "tensor memory budget");
@@ -81,10 +87,10 @@ struct PrefillTmCfg {
   static_assert(!F8 || D == 64 || D == 128, "fp8 caches: head_dim 64 or 128");
 };
 
-template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
-__global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
+template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false, int SW = 1>
+__global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     ua_prefill_tm_kernel(const __grid_constant__ PrefillParams pp) {
-  using C = PrefillTmCfg<D, NQ, F8>;
+  using C = PrefillTmCfg<D, NQ, F8, SW>;
   constexpr int BN = C::kBN;
   constexpr int RK = C::kRingK, RV = C::kRingV;
   constexpr int kProducerK = C::kSoftmaxWarps, kProducerV = C::kSoftmaxWarps + 1;
@@ -122,6 +128,10 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
   uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(tile_bars + 3 * NQ);
   // [NQ][2]: walk step + 1 of the tile's P when its low part matters
   int* const lo_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  // SW > 1: per (q tile, lane quarter) a barrier for the tile's row-max exchange and one for
+  // the final row-sum exchange ([NQ][4][2]), and the exchanged values
+  uint64_t* const xch_bars = reinterpret_cast<uint64_t*>(lo_flag + 2 * NQ + 1);  // 8-byte aligned
+  float* const xch = reinterpret_cast<float*>(bars) + C::kBarBytes / 4;  // [NQ][SW][3][128]
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
@@ -183,9 +193,11 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
       mbar_init(v8_full, 1);
       mbar_init(v8_empty, C::kDeqWarps);
     }
+    if constexpr (SW > 1)
+      for (int i = 0; i < NQ * 4 * 2; ++i) mbar_init(&xch_bars[i], 32 * SW);
     for (int qt = 0; qt < NQ; ++qt) {
       mbar_init(s_full(qt), 1);
-      mbar_init(p_full(qt), 4);
+      mbar_init(p_full(qt), 4 * SW);
       mbar_init(pv_done(qt), 1);
       lo_flag[2 * qt] = lo_flag[2 * qt + 1] = 0;
     }
@@ -376,6 +388,22 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
     fence_proxy_async_smem();  // generic writes, read by the tensor cores
     __syncwarp();
     if (lane == 0) mbar_arrive(q_ready);
+    // per-token scales: each key's K (V) row is written times its own scale, rounded once
+    // to f16 (0 for keys past the partition's walk)
+    const bool tok = p.k_scale_tok != nullptr;
+    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    auto key_scale = [&](int j, int op) -> float {
+      const int key = ks + j * BN + td;
+      if (key >= ke) return 0.f;
+      const int col = key / p.block_size;
+      const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+      if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) return 0.f;
+      const long long slot = key % p.block_size;
+      return op == 0 ? __ldg(p.k_scale_tok + blk * p.k_scale_stride[0] +
+                             slot * p.k_scale_stride[1] + g * p.k_scale_stride[2])
+                     : __ldg(p.v_scale_tok + blk * p.v_scale_stride[0] +
+                             slot * p.v_scale_stride[1] + g * p.v_scale_stride[2]);
+    };
 #pragma unroll 1
     for (int j = 0; ok && j < nt; ++j) {
 #pragma unroll 1
@@ -383,6 +411,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
         const int R = op ? RV : RK;
         uint64_t* const f8_full = op ? v8_full : k8_full;
         uint64_t* const f8_empty = op ? v8_empty : k8_empty;
+        const float ts = tok ? key_scale(j, op) : 1.f;
         if (!pf_wait_warp(f8_full, j & 1, abort_flag, p.status)) { ok = false; break; }
         // take the row of codes into registers and hand the staging tile back at once, so
         // the next tile's copy overlaps the conversion
@@ -417,9 +446,13 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
           const uint32_t w[4] = {r.x, r.y, r.z, r.w};
           uint32_t h[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            h[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q]));
-            h[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16));
+          for (int q = 0; q < 4; ++q) e4m3x4_to_f16x4(w[q], h[2 * q], h[2 * q + 1]);
+          if (tok) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[q]));
+              h[q] = pack_f16(f.x * ts, f.y * ts);
+            }
           }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -435,9 +468,17 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
     }
   } else {
     // ======================================================== softmax warps (thread = row)
-    const int qt = warp >> 2;                              // q tile of this warp
+    // SW warps share a tensor-memory lane quarter: warp `half` takes S columns
+    // [half BN / SW, (half + 1) BN / SW) of every key tile and O columns
+    // [half D / SW, (half + 1) D / SW); their row maxima meet in shared memory once per
+    // tile (the same running max in every warp of a row), their row sums at the end.
+    constexpr int kCols = BN / SW, kOCols = D / SW;
+    const int qt = warp / (4 * SW);                        // q tile of this warp
     const int quad = warp & 3;                             // its tensor-memory lane quarter
+    const int half = (warp % (4 * SW)) >> 2;               // its column slice
     const int r = 32 * quad + lane;                        // row within the q tile
+    uint64_t* const xbar = xch_bars + 2 * (4 * qt + quad);  // [0]: row max, [1]: row sum
+    float* const xrow = xch + (qt * SW) * 3 * 128 + r;      // + (h * 3 + slot) * 128
     int jb, je;
     tile_walk(qt, jb, je);
     const int n_tiles = je - jb;
@@ -467,12 +508,14 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
     // the row max is taken on the raw dot products and the scale folds into the exponent's
     // FMA.  Otherwise scores are transformed first and c = log2(e).
     // fp8: the per-tensor k_scale joins the score scale, v_scale the output
-    const float kq = F8 ? p.scale * __ldg(p.kv_scale) : p.scale;
-    const float v_mul = F8 ? __ldg(p.kv_scale + 1) : 1.f;
+    // (per-token scales are already in the f16 tiles)
+    const bool tok8 = F8 && p.k_scale_tok != nullptr;
+    const float kq = F8 && !tok8 ? p.scale * __ldg(p.kv_scale) : p.scale;
+    const float v_mul = F8 && !tok8 ? __ldg(p.kv_scale + 1) : 1.f;
     const float c = FEAT ? kLog2e : kq * kLog2e;
     const bool sink = p.sinks != nullptr && z == 0 && rv;
     float m_used = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
-    float l = sink ? 1.f : 0.f;
+    float l = sink && half == 0 ? 1.f : 0.f;  // the sink's share, counted once per row
     const uint32_t tS = tmem + qt * C::kTmemStride + ((32u * quad) << 16);
     const uint32_t tO = tS + BN;
     bool ok = true;
@@ -503,7 +546,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
       const bool rewrite = FEAT || need_mask;
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 64) {
+      for (int c0 = half * kCols; c0 < (half + 1) * kCols; c0 += 64) {
         uint32_t ra[32], rb[32];
         tmem_ld32(tS + c0, ra);
         tmem_ld32(tS + c0 + 32, rb);
@@ -532,7 +575,15 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
         }
       }
       if (rewrite) tmem_st_wait();
-      const float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
+      float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
+      if constexpr (SW > 1) {
+        // the row's other column slices: every lane arrives once its value is written
+        xrow[(half * 3 + (n & 1)) * 128] = mx;
+        mbar_arrive(&xbar[0]);
+        if (!pf_wait_warp(&xbar[0], n & 1, abort_flag, p.status)) { ok = false; break; }
+#pragma unroll
+        for (int hh = 0; hh < SW; ++hh) mx = fmaxf(mx, xrow[(hh * 3 + (n & 1)) * 128]);
+      }
       // ---- running max, used lazily: O and l are rescaled only when the max grows by
       // more than 8 in log2 units (P stays <= 256, far inside the fp32 and P ranges)
       float alpha = 1.f;
@@ -545,7 +596,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
       // O holds P.V of step n-1 (its commit preceded this step's S): rescale it in place
       if (n >= 1 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = half * kOCols; c0 < (half + 1) * kOCols; c0 += 32) {
           uint32_t rr[32];
           tmem_ld32(tO + c0, rr);
           tmem_ld_wait();
@@ -564,7 +615,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
       const float2 cc = make_float2(c, c), mm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = half * kCols; c0 < (half + 1) * kCols; c0 += 32) {
         uint32_t rr[32];
         tmem_ld32(tS + c0, rr);
         tmem_ld_wait();
@@ -606,13 +657,23 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
 
     // ---- epilogue: O / l for one partition, or the partition's max / sum / O
     if (ok && n_tiles > 0) ok = pf_wait_warp(pv_done(qt), 0, abort_flag, p.status);
+    if constexpr (SW > 1) {
+      if (ok) {  // the row sum over every column slice
+        xrow[(half * 3 + 2) * 128] = l;
+        mbar_arrive(&xbar[1]);
+        ok = pf_wait_warp(&xbar[1], 0, abort_flag, p.status);
+        l = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < SW; ++hh) l += xrow[(hh * 3 + 2) * 128];
+      }
+    }
     tc_fence_after();
     if (ok) {
       const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
       const size_t n_part = static_cast<size_t>(p.n_part);
       const float inv = l > 0.f ? v_mul / l : 0.f;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = half * kOCols; c0 < (half + 1) * kOCols; c0 += 32) {
         uint32_t rr[32];
         if (n_tiles > 0) {
           tmem_ld32(tO + c0, rr);
@@ -664,10 +725,13 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8>::kThreads, 1)
   if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// One q tile a CTA: two softmax warps per lane quarter (a CTA would otherwise have one
+// softmax warp per SM sub-partition); two q tiles already alternate on the tensor cores.
 template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
 cudaError_t launch_prefill_tm_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
-  using C = PrefillTmCfg<D, NQ, F8>;
-  auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT, F8>;
+  constexpr int SW = NQ == 1 ? 2 : 1;
+  using C = PrefillTmCfg<D, NQ, F8, SW>;
+  auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT, F8, SW>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);

@@ -43,7 +43,12 @@
 
 namespace ua {
 
-template <int D>
+// F8: fp8-e4m3 caches.  The producers copy each half tile of codes (128 keys x 128 bytes)
+// into a two-slot staging ring, and four dequant warps (thread = key) write it into its f16
+// slot, exactly (every e4m3 value is an f16), so the f16 MMAs and the softmax run
+// unchanged; k_scale joins the score scale and v_scale the output (per-token scales:
+// folded into each key's f16 row instead).
+template <int D, bool F8 = false>
 struct PrefillWideCfg {
   static constexpr int kBM = 128;                   // MMA rows of the q tile
   static constexpr int kBN = 128;                   // keys per tile
@@ -52,15 +57,24 @@ struct PrefillWideCfg {
   static constexpr int kSlotCB = 2;                 // column blocks of one half tile
   static constexpr int kSlotCBBytes = kBN * 128;    // one column block of a half tile
   static constexpr int kSlotBytes = kSlotCB * kSlotCBBytes;
-  static constexpr int kSlots = 5;
+  static constexpr int kSlots = F8 ? 4 : 5;         // f16 half tiles
+  static constexpr int kStage = F8 ? 2 : 0;         // fp8: staging slots of codes
+  static constexpr int kStageBytes = kBN * 128;     // one staged half tile of codes
   static constexpr int kBarBytes = 512;
-  static constexpr int kSmemBytes = 1024 + kQBytes + kSlots * kSlotBytes + kBarBytes;
+  static constexpr int kSmemBytes =
+      1024 + kQBytes + kSlots * kSlotBytes + kStage * kStageBytes + kBarBytes;
   static constexpr int kTmemCols = 512;             // S0, S1, O
-  static constexpr int kProducers = 4;              // TMA producer warps
-  static constexpr int kThreads = 32 * (4 + kProducers + 1);
+  // TMA producer warps: a 16-bit half tile is 16 page boxes, an fp8 one 8.  Each producer
+  // reuses the staging slot of its own previous item, so the fp8 staging ring holds as many
+  // items as there are producers (a producer's parity wait is then never more than one
+  // phase behind).
+  static constexpr int kProducers = F8 ? 2 : 4;
+  static constexpr int kDeqWarps = F8 ? 4 : 0;
+  static constexpr int kThreads = 32 * (4 + kProducers + 1 + kDeqWarps);
   static_assert(D == 256, "two half tiles of 128 columns");
   static_assert(2 * kBN + D <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(!F8 || kStage == kProducers, "one staging slot per producer warp");
 };
 
 // Position of half h of K tile j and of V tile j in the slot sequence
@@ -70,12 +84,15 @@ __device__ __forceinline__ int wide_item_v(int j, int h, int nt) {
   return j < nt - 1 ? 4 * j + 4 + h : 4 * j + 2 + h;
 }
 
-template <int D, bool BF16, bool FEAT>
-__global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
+template <int D, bool BF16, bool FEAT, bool F8 = false>
+__global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
     ua_prefill_wide_kernel(const __grid_constant__ PrefillParams pp) {
-  using C = PrefillWideCfg<D>;
+  using C = PrefillWideCfg<D, F8>;
   constexpr int BN = C::kBN;
   constexpr int NS = C::kSlots;
+  constexpr int kMma = 4 + C::kProducers;
+  constexpr int kDeq0 = kMma + 1;  // fp8: dequant warps kDeq0 .. kDeq0 + 3
+  static_assert(!F8 || !BF16, "fp8 caches run the f16 MMAs");
   const AttnParams& p = pp.p;
   grid_dependency_wait();
   grid_launch_dependents();
@@ -85,7 +102,8 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* const sQ = smem;
   uint8_t* const sR = sQ + C::kQBytes;                // NS slots
-  uint64_t* const bars = reinterpret_cast<uint64_t*>(sR + NS * C::kSlotBytes);
+  uint8_t* const s8 = sR + NS * C::kSlotBytes;         // fp8: staging slots of codes
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(s8 + C::kStage * C::kStageBytes);
   uint64_t* const q_full = bars + 0;
   uint64_t* const fin = bars + 1;
   uint64_t* const pv_done = bars + 2;                 // one phase per P.V_j
@@ -94,7 +112,11 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
   uint64_t* const full = bars + 7;                    // [NS]
   uint64_t* const empty = full + NS;                  // [NS]
   uint64_t* const lo_bar = empty + NS;                // the softmax warps agree on P's low part
-  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(lo_bar + 1);
+  // fp8: Q converted (dequant warps), staging slot full (copies) and empty (dequant warps)
+  uint64_t* const q_ready = lo_bar + 1;
+  uint64_t* const s8_full = q_ready + 1;              // [kStage]
+  uint64_t* const s8_empty = s8_full + C::kStage;     // [kStage]
+  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(s8_empty + C::kStage);
   int* const lo_flag = reinterpret_cast<int*>(tmem_holder + 1);  // [2]: step + 1 when P_lo matters
   __shared__ int s_abort;
   __shared__ int s_last[C::kProducers];  // last item each producer warp issued
@@ -136,8 +158,15 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
       lo_flag[i] = 0;
     }
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&full[i], F8 ? C::kDeqWarps : 1);  // f16 slots: written by the copies or
+      mbar_init(&empty[i], 1);                      // (fp8) the dequant warps
+    }
+    if constexpr (F8) {
+      mbar_init(q_ready, C::kDeqWarps);
+      for (int i = 0; i < C::kStage; ++i) {
+        mbar_init(&s8_full[i], 1);
+        mbar_init(&s8_empty[i], C::kDeqWarps);
+      }
     }
     s_abort = 0;
     mbar_fence_init();
@@ -152,7 +181,7 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
     }
   }
   fence_proxy_async_smem();
-  if (warp == 4 + C::kProducers) {
+  if (warp == kMma) {
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
@@ -166,13 +195,17 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
   if (warp >= 4 && warp < 4 + C::kProducers) {
     // ======================================================== TMA producers
     // Producer warp pw issues the items u = pw, pw + NP, ... of the slot sequence; lane
-    // i < 16 issues page i / 2 (16 keys), column block i % 2 of the item's half tile.
+    // i < 16 issues page i / 2 (16 keys), column block i % 2 of the item's half tile
+    // (fp8: lane i < 8 page i, the half tile's one 128-byte column block, into the staging
+    // slot u % NP).
     constexpr int NP = C::kProducers;
+    constexpr int NR = F8 ? C::kStage : NS;  // slots this warp's copies land in
     const int pw = warp - 4;
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
     const int bs = p.block_size;
     const int oob = p.num_blocks * bs;
-    const int page = lane >> 1, cbl = lane & 1;
+    const int page = F8 ? lane : lane >> 1, cbl = F8 ? 0 : lane & 1;
+    constexpr int kBoxLanes = F8 ? 8 : 16;
     if (pw == 0 && lane == 0) {
       mbar_arrive_expect_tx(q_full, C::kCB * TQ * G * 128);
       for (int cb = 0; cb < C::kCB; ++cb)
@@ -194,11 +227,11 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
     auto page_blk = [&](int j) -> int {
       const int key = ks + j * BN + 16 * page;
       const int col = key / bs;
-      return (j < nt && lane < 16 && key < ke && col < p.max_blocks_per_seq) ? __ldg(bt + col) : -1;
+      return (j < nt && lane < kBoxLanes && key < ke && col < p.max_blocks_per_seq) ? __ldg(bt + col) : -1;
     };
     auto page_row = [&](int j, int blk) -> int {
       const int key = ks + j * BN + 16 * page;
-      if (lane >= 16 || key >= ke) return oob;
+      if (lane >= kBoxLanes || key >= ke) return oob;
       if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
         atomicOr(p.status, DEV_BAD_BLOCK);
         return oob;
@@ -222,13 +255,20 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
         decode(u + NP, k2, j2, h2);
         blk_cur = page_blk(j2);
       }
-      const int sl = u % NS;
-      if (u >= NS && !pf_wait_warp(&empty[sl], ((u / NS) - 1) & 1, abort_flag, p.status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&full[sl], C::kSlotBytes);
+      const int sl = u % NR;
+      uint64_t* const f = F8 ? &s8_full[sl] : &full[sl];
+      uint64_t* const e = F8 ? &s8_empty[sl] : &empty[sl];
+      if (u >= NR && !pf_wait_warp(e, ((u / NR) - 1) & 1, abort_flag, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(f, F8 ? C::kStageBytes : C::kSlotBytes);
       __syncwarp();
-      if (lane < 16)
-        tma_load_3d_pf(sR + sl * C::kSlotBytes + cbl * C::kSlotCBBytes + page * 2048,
-                       is_k ? &pp.tmap_k : &pp.tmap_v, 64 * (2 * h + cbl), g, row, &full[sl]);
+      if (lane < kBoxLanes) {
+        if constexpr (F8)
+          tma_load_3d_pf(s8 + sl * C::kStageBytes + page * 2048, is_k ? &pp.tmap_k : &pp.tmap_v,
+                         128 * h, g, row, f);
+        else
+          tma_load_3d_pf(sR + sl * C::kSlotBytes + cbl * C::kSlotCBBytes + page * 2048,
+                         is_k ? &pp.tmap_k : &pp.tmap_v, 64 * (2 * h + cbl), g, row, f);
+      }
       last = u;
     }
     // Never leave copies in flight into this CTA's shared memory (even after an abort).
@@ -237,15 +277,16 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
     // its warp's last item is at least u + NS.
     if (lane == 0) s_last[pw] = last;
     named_bar_sync(2, 32 * NP);
-    for (int u = last; u >= 0 && u > last - NS; u -= NP)
-      if (s_last[(u + NS) % NP] < u + NS)
-        mbar_wait_bounded(&full[u % NS], (u / NS) & 1, p.status, DEV_TIMEOUT);
+    for (int u = last; u >= 0 && u > last - NR; u -= NP)
+      if (s_last[(u + NR) % NP] < u + NR)
+        mbar_wait_bounded(F8 ? &s8_full[u % NR] : &full[u % NR], (u / NR) & 1, p.status,
+                          DEV_TIMEOUT);
     if (pw == 0 && lane == 0) mbar_wait_bounded(q_full, 0, p.status, DEV_TIMEOUT);
-  } else if (warp == 4 + C::kProducers) {
+  } else if (warp == kMma) {
     // ======================================================== MMA issuer (converged warp)
     constexpr uint32_t kIdQK = umma_idesc_f16(128, BN, BF16, false);
     constexpr uint32_t kIdPV = umma_idesc_f16(128, 128, BF16, true);
-    bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
+    bool ok = pf_wait_warp(F8 ? q_ready : q_full, 0, abort_flag, p.status);
     auto qk = [&](int j) -> bool {
       const uint32_t tS = tmem + (j & 1) * BN;
 #pragma unroll
@@ -278,8 +319,9 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
         if (!pf_wait_warp(&full[sl], (u / NS) & 1, abort_flag, p.status)) return false;
         uint8_t* vs = sR + sl * C::kSlotBytes;
         // Cache slots at or past kv_len hold no key and may hold anything (NaN included):
-        // zero those V rows before the tensor cores multiply them by P = 0.
-        if (k0 + BN > kv_len) {
+        // zero those V rows before the tensor cores multiply them by P = 0 (fp8: the
+        // dequant warps wrote them as zeros).
+        if (!F8 && k0 + BN > kv_len) {
           const int r_lo = max(0, kv_len - k0), r_hi = min(BN, ((kv_len + 15) & ~15) - k0);
           for (int e = lane; e < (r_hi - r_lo) * C::kSlotCB * 8; e += 32) {
             const int r = r_lo + e / (C::kSlotCB * 8), c = e % (C::kSlotCB * 8);
@@ -314,6 +356,106 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
     // nothing may still be in flight on the tensor cores when the memory is freed
     umma_commit_warp(fin);
     mbar_wait_bounded(fin, 0, p.status, DEV_TIMEOUT);
+  } else if (F8 && warp >= kDeq0) {
+    // ======================================================== fp8 dequant warps (thread = key)
+    // Q (bf16) to f16 in place once; then every item of the slot sequence: the staged half
+    // tile of codes (128-byte rows, 128-byte swizzled) into its f16 slot (two 128-byte
+    // swizzled column blocks), each e4m3 value exactly, or times the key's own scale
+    // (per-token scales); V rows of keys at or past kv_len become zeros.
+    const int td = (warp - kDeq0) * 32 + lane;
+    const uint32_t sw = td & 7;
+    bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
+    if (ok && p.q_dtype == UA_DT_BF16) {
+#pragma unroll 1
+      for (int cb = 0; cb < C::kCB; ++cb) {
+        uint4* row = reinterpret_cast<uint4*>(sQ + cb * C::kBM * 128 + td * 128);
+#pragma unroll
+        for (int c0 = 0; c0 < 8; ++c0) {  // element-wise: the order only spreads the banks
+          const int c = c0 ^ static_cast<int>(sw);
+          uint4 v = row[c];
+          v.x = pack_f16(bf16_lo(v.x), bf16_hi(v.x));
+          v.y = pack_f16(bf16_lo(v.y), bf16_hi(v.y));
+          v.z = pack_f16(bf16_lo(v.z), bf16_hi(v.z));
+          v.w = pack_f16(bf16_lo(v.w), bf16_hi(v.w));
+          row[c] = v;
+        }
+      }
+    }
+    fence_proxy_async_smem();  // generic writes, read by the tensor cores
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_ready);
+    const bool tok = p.k_scale_tok != nullptr;
+    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    // the per-token scale of this thread's key of tile j (0 past the partition's keys)
+    auto key_scale = [&](int j, bool is_k) -> float {
+      const int key = ks + j * BN + td;
+      if (key >= ke) return 0.f;
+      const int col = key / p.block_size;
+      const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+      if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) return 0.f;
+      const long long slot = key % p.block_size;
+      return is_k ? __ldg(p.k_scale_tok + blk * p.k_scale_stride[0] + slot * p.k_scale_stride[1] +
+                          g * p.k_scale_stride[2])
+                  : __ldg(p.v_scale_tok + blk * p.v_scale_stride[0] + slot * p.v_scale_stride[1] +
+                          g * p.v_scale_stride[2]);
+    };
+    const int n_items = 4 * nt;
+#pragma unroll 1
+    for (int u = 0; ok && u < n_items; ++u) {
+      bool is_k;
+      int j, h;
+      if (u < 2) {
+        is_k = true, j = 0, h = u;
+      } else {
+        const int v = u - 2, blk4 = v >> 2, r = v & 3;
+        is_k = blk4 < nt - 1 && r < 2;
+        j = is_k ? blk4 + 1 : blk4;
+        h = r & 1;
+      }
+      const float ts = tok ? key_scale(j, is_k) : 1.f;
+      const int st = u % C::kStage;
+      if (!pf_wait_warp(&s8_full[st], (u / C::kStage) & 1, abort_flag, p.status)) { ok = false; break; }
+      // take the row of codes into registers and hand the staging slot back at once
+      uint4 raw[8];
+      {
+        const uint8_t* src = s8 + st * C::kStageBytes + td * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s8_empty[st]);
+      const int sl = u % NS;
+      if (u >= NS && !pf_wait_warp(&empty[sl], ((u / NS) - 1) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* dst = sR + sl * C::kSlotBytes + td * 128;
+      const bool zero = !is_k && ks + j * BN + td >= kv_len;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {  // 16 codes of the row -> f16 chunks 2c, 2c + 1
+        const uint4 r = zero ? make_uint4(0, 0, 0, 0) : raw[c];
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+        uint32_t hh[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) e4m3x4_to_f16x4(w[q], hh[2 * q], hh[2 * q + 1]);
+        if (tok) {  // the key's scale, rounded once to f16 with each value
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[q]));
+            hh[q] = pack_f16(f.x * ts, f.y * ts);
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < 2; ++uu) {
+          const int cc = 2 * c + uu;  // f16 chunk of the row: column block cc / 8
+          *reinterpret_cast<uint4*>(dst + (cc >> 3) * C::kSlotCBBytes + (((cc & 7) ^ sw) << 4)) =
+              make_uint4(hh[4 * uu], hh[4 * uu + 1], hh[4 * uu + 2], hh[4 * uu + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[sl]);
+    }
   } else {
     // ======================================================== softmax warps (thread = row)
     const int r = 32 * warp + lane;
@@ -337,7 +479,12 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
       if (p.qq_bias != nullptr && rv && i_q < p.max_seqlen_q)
         qq_row = p.qq_bias + static_cast<size_t>(i_q) * p.qq_stride;
     }
-    const float c = FEAT ? kLog2e : p.scale * kLog2e;
+    // fp8: the per-tensor k_scale joins the score scale, v_scale the output (per-token
+    // scales are already in the f16 tiles)
+    const bool tok8 = F8 && p.k_scale_tok != nullptr;
+    const float kq = F8 && !tok8 ? p.scale * __ldg(p.kv_scale) : p.scale;
+    const float v_mul = F8 && !tok8 ? __ldg(p.kv_scale + 1) : 1.f;
+    const float c = FEAT ? kLog2e : kq * kLog2e;
     const bool sink = p.sinks != nullptr && z == 0 && rv;
     float m_used = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
     float l = sink ? 1.f : 0.f;
@@ -347,7 +494,7 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
 
     auto score = [&](float v, int jk, auto mask) -> float {
       if constexpr (FEAT) {
-        v *= p.scale;
+        v *= kq;
         if (p.softcap > 0.f) v = p.softcap * fast_tanh(v * inv_softcap);
         v += slope * static_cast<float>(jk - ctx);
         if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
@@ -491,7 +638,7 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
     if (ok) {
       const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
       const size_t n_part = static_cast<size_t>(p.n_part);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? v_mul / l : 0.f;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t rr[32];
@@ -533,8 +680,8 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
           float4* dst = reinterpret_cast<float4*>(p.ws_acc + w * D + c0);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
-                                 __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+            dst[e] = make_float4(__uint_as_float(rr[4 * e]) * v_mul, __uint_as_float(rr[4 * e + 1]) * v_mul,
+                                 __uint_as_float(rr[4 * e + 2]) * v_mul, __uint_as_float(rr[4 * e + 3]) * v_mul);
         }
       }
     }
@@ -542,13 +689,13 @@ __global__ void __launch_bounds__(PrefillWideCfg<D>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4 + C::kProducers) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D, bool BF16, bool FEAT>
+template <int D, bool BF16, bool FEAT, bool F8 = false>
 cudaError_t launch_prefill_wide_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
-  using C = PrefillWideCfg<D>;
-  auto kern = ua_prefill_wide_kernel<D, BF16, FEAT>;
+  using C = PrefillWideCfg<D, F8>;
+  auto kern = ua_prefill_wide_kernel<D, BF16, FEAT, F8>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -571,6 +718,9 @@ cudaError_t launch_prefill_wide_dispatch(const PrefillParams& pp, dim3 grid, int
   if (kv == KV_F16)
     return feat ? launch_prefill_wide_t<D, false, true>(pp, grid, s)
                 : launch_prefill_wide_t<D, false, false>(pp, grid, s);
+  if (kv == KV_E4M3)
+    return feat ? launch_prefill_wide_t<D, false, true, true>(pp, grid, s)
+                : launch_prefill_wide_t<D, false, false, true>(pp, grid, s);
   return cudaErrorInvalidValue;
 }
 

@@ -249,9 +249,13 @@ PREFILL_D128_FP8 = replace(PREFILL_D128, name="prefill_d128_fp8", kv_dtype=torch
 PREFILL_D256 = replace(PREFILL_D128, name="prefill_d256", num_q_heads=24, num_kv_heads=4,
                        head_dim=256,
                        desc="4x4096 prompts + 2048 chunk behind 16384 prefix; 24q/4kv d256; bf16")
+PREFILL_D256_FP8 = replace(PREFILL_D256, name="prefill_d256_fp8", kv_dtype=torch.float8_e4m3fn,
+                           desc="4x4096 prompts + 2048 chunk behind 16384 prefix; 24q/4kv d256; "
+                                "bf16 q, fp8 e4m3 KV")
 
 WORKLOADS = {s.name: s for s in (TINY, DECODE, MIXED, SWDECODE_BF16, SWDECODE_FP8,
-                                 SWDECODE_FP8_TOK, PREFILL_D128, PREFILL_D128_FP8, PREFILL_D256)}
+                                 SWDECODE_FP8_TOK, PREFILL_D128, PREFILL_D128_FP8, PREFILL_D256,
+                                 PREFILL_D256_FP8)}
 
 
 def kv_bytes_read(inp: Inputs) -> int:
