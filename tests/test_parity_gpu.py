@@ -455,6 +455,18 @@ def test_per_token_scales_on_the_tile_kernel_are_unsupported():
         run(replace(inp, v_scale_tok=None))
 
 
+def test_both_decode_tile_widths_run():
+    """The decode parity cases reach both widths of the decode tile on this device: four
+    consumer warps (three CTAs an SM) on the sliding-window decode, eight (one CTA an SM)
+    on a small decode grid."""
+    assert _plan(inputs(W.SWDECODE_BF16))["kernel"] == 2
+    spec = _small(100 + sorted(SMALL).index("dec_fp8_feat"), **SMALL["dec_fp8_feat"])
+    inp = W.make(spec, poison=True)
+    assert _plan(inp, "2d")["kernel"] == 32
+    want = oracle.attention(threads=THREADS, **inp.oracle_kwargs())
+    assert max_err(run(inp, backend="2d"), want) <= TOL[spec.kv_dtype]
+
+
 def test_out_of_range_block_id_is_reported_not_read():
     inp = W.make(_small(9))
     bt = inp.block_table.clone()

@@ -55,9 +55,6 @@ struct DecCfg {
                                       ? kStages * kStageBytes
                                       : kMergeBytes + kPartBytes;
   static constexpr int kPipeBytes = (kPipeRaw + 1023) & ~1023;
-  // Stages whose pages are requested into L2 ahead of the shared-memory ring, so more of
-  // the walk's DRAM reads are in flight than the ring holds.
-  static constexpr int kPrefetch = 4;
   // fp8 per-token scales of a stage's keys, K then V, behind the barriers
   static constexpr int kScaleBytes = kPermD ? kStages * 2 * kT * 4 : 0;
   static constexpr int kSmemBytes = 1024 + kPipeBytes + 2 * kStages * 8 + kScaleBytes;
@@ -198,27 +195,12 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
       if (ntiles > 0) load_scales(0, scale_blk(0), sc_next);
       blk_next = scale_blk(1);
     }
-    // L2 prefetch of tile t's pages (lanes < W), kept kPrefetch tiles ahead of the ring
-    auto prefetch = [&](int t) {
-      if (t >= ntiles) return;
-      const int prow = page_row(t);
-      if (lane < T / 16 && prow != oob) {
-#pragma unroll
-        for (int cb = 0; cb < C::kCB; ++cb) {
-          const int x = cb * (C::kCBW / C::kEsz);
-          tma_prefetch_l2_3d(&tp.tmap_k, x, g, prow);
-          tma_prefetch_l2_3d(&tp.tmap_v, x, g, prow);
-        }
-      }
-    };
-    for (int t = S; t < S + C::kPrefetch - 1; ++t) prefetch(t);
     int issued = 0;
     int row_next = ntiles > 0 ? page_row(0) : oob;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % S;
       const int row = row_next;
       if (t + 1 < ntiles) row_next = page_row(t + 1);  // block-table lookups one tile ahead
-      prefetch(t + S + C::kPrefetch - 1);
       float sc_cur[KPL][2];
 #pragma unroll
       for (int e = 0; e < KPL; ++e) {

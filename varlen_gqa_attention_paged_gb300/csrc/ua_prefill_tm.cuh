@@ -65,9 +65,9 @@ struct PrefillTmCfg {
   static constexpr int kF8Tile = kBN * D;
   static constexpr int kF8Bytes = F8 ? 2 * kF8Tile : 0;
   static constexpr int kDeqWarps = F8 ? 4 : 0;
-  // SW > 1: the row maxima of each tile (two buffers) and the final row sums of the SW
-  // warps of a row, exchanged through shared memory
-  static constexpr int kXchBytes = SW > 1 ? NQ * SW * 3 * 128 * 4 : 0;
+  // SW > 1: each tile's row maxima of the SW warps of a row, exchanged through shared
+  // memory as bf16 values rounded up
+  static constexpr int kXchBytes = SW > 1 ? NQ * SW * 128 * 2 : 0;
   // K and V ring depths: as many tiles as fit beside Q (K gets the odd one, at most 4 each)
   static constexpr int kSlots =
       (227 * 1024 - 1024 - kBarBytes - NQ * kQBytes - kF8Bytes - kXchBytes) / kTileBytes;
@@ -129,9 +129,9 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   // [NQ][2]: walk step + 1 of the tile's P when its low part matters
   int* const lo_flag = reinterpret_cast<int*>(tmem_holder + 1);
   // SW > 1: per (q tile, lane quarter) a barrier for the tile's row-max exchange and one for
-  // the final row-sum exchange ([NQ][4][2]), and the exchanged values
+  // the final row-sum exchange ([NQ][4][2]), and the exchanged maxima
   uint64_t* const xch_bars = reinterpret_cast<uint64_t*>(lo_flag + 2 * NQ + 1);  // 8-byte aligned
-  float* const xch = reinterpret_cast<float*>(bars) + C::kBarBytes / 4;  // [NQ][SW][3][128]
+  uint16_t* const xch = reinterpret_cast<uint16_t*>(bars) + C::kBarBytes / 2;  // [NQ][SW][128]
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
@@ -470,21 +470,26 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     // ======================================================== softmax warps (thread = row)
     // SW warps share a tensor-memory lane quarter: warp `half` takes S columns
     // [half BN / SW, (half + 1) BN / SW) of every key tile and O columns
-    // [half D / SW, (half + 1) D / SW); their row maxima meet in shared memory once per
-    // tile (the same running max in every warp of a row), their row sums at the end.
+    // [half D / SW, (half + 1) D / SW).  Once per tile their row maxima meet in shared
+    // memory, each rounded up to bf16, and every warp of the row takes the largest: the
+    // same running max in every warp, never below the true one.  Their row sums meet at
+    // the end through two columns of the tile's S/P region, free after its last P.V.
     constexpr int kCols = BN / SW, kOCols = D / SW;
     const int qt = warp / (4 * SW);                        // q tile of this warp
     const int quad = warp & 3;                             // its tensor-memory lane quarter
     const int half = (warp % (4 * SW)) >> 2;               // its column slice
     const int r = 32 * quad + lane;                        // row within the q tile
     uint64_t* const xbar = xch_bars + 2 * (4 * qt + quad);  // [0]: row max, [1]: row sum
-    float* const xrow = xch + (qt * SW) * 3 * 128 + r;      // + (h * 3 + slot) * 128
+    uint16_t* const xrow = xch + (qt * SW) * 128 + r;       // + h * 128
     int jb, je;
     tile_walk(qt, jb, je);
     const int n_tiles = je - jb;
     const int tf = t_first + qt * TQ;
     const int tl = r / G;                                  // token within the q tile
     const bool rv = qt < nq_act && r < TQ * G && tf + tl < q_len && q0 + tf + tl < p.total_q;
+    // a warp none of whose rows holds a query row (a q tile's unused rows) only keeps the
+    // tile barriers in step: what its rows of P and O hold is never stored
+    const bool active = __any_sync(0xffffffffu, rv);
     const int i_q = tf + (rv ? tl : 0);                    // query index within the sequence
     const int h = g * G + r % G;
     const int pos = ctx + i_q;
@@ -538,6 +543,12 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     for (int n = 0; n < n_tiles; ++n) {
       if (!pf_wait_warp(s_full(qt), n & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
+      if (!active) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(qt));
+        continue;
+      }
       const int k0 = ks + (jb + n) * BN;
       const bool need_mask = k0 < lomax || k0 + BN - 1 > pmin || k0 + BN > ke;
 
@@ -577,12 +588,18 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       if (rewrite) tmem_st_wait();
       float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
       if constexpr (SW > 1) {
-        // the row's other column slices: every lane arrives once its value is written
-        xrow[(half * 3 + (n & 1)) * 128] = mx;
+        // the row's other column slices: every lane arrives once its value is written.  The
+        // buffer is rewritten for tile n + 1 only after every warp's P of tile n (its S
+        // wait follows the P.V that waited for them), so one buffer serves every tile.
+        const uint32_t u = __float_as_uint(mx);
+        xrow[half * 128] = static_cast<uint16_t>(
+            ((u & 0xFFFFu) == 0u || (u >> 31)) ? (u >> 16) : (u >> 16) + 1u);  // round up
         mbar_arrive(&xbar[0]);
         if (!pf_wait_warp(&xbar[0], n & 1, abort_flag, p.status)) { ok = false; break; }
+        mx = -INFINITY;
 #pragma unroll
-        for (int hh = 0; hh < SW; ++hh) mx = fmaxf(mx, xrow[(hh * 3 + (n & 1)) * 128]);
+        for (int hh = 0; hh < SW; ++hh)
+          mx = fmaxf(mx, __uint_as_float(static_cast<uint32_t>(xrow[hh * 128]) << 16));
       }
       // ---- running max, used lazily: O and l are rescaled only when the max grows by
       // more than 8 in log2 units (P stays <= 256, far inside the fp32 and P ranges)
@@ -657,17 +674,21 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
 
     // ---- epilogue: O / l for one partition, or the partition's max / sum / O
     if (ok && n_tiles > 0) ok = pf_wait_warp(pv_done(qt), 0, abort_flag, p.status);
+    tc_fence_after();
     if constexpr (SW > 1) {
-      if (ok) {  // the row sum over every column slice
-        xrow[(half * 3 + 2) * 128] = l;
+      if (ok && active) {  // the row sum over every column slice, through tensor memory
+        tmem_st1(tS + half, __float_as_uint(l));
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(&xbar[1]);
         ok = pf_wait_warp(&xbar[1], 0, abort_flag, p.status);
-        l = 0.f;
-#pragma unroll
-        for (int hh = 0; hh < SW; ++hh) l += xrow[(hh * 3 + 2) * 128];
+        tc_fence_after();
+        uint32_t l0, l1;
+        tmem_ld2(tS, l0, l1);
+        tmem_ld_wait();
+        l = __uint_as_float(l0) + __uint_as_float(l1);
       }
     }
-    tc_fence_after();
     if (ok) {
       const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
       const size_t n_part = static_cast<size_t>(p.n_part);
@@ -725,11 +746,12 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// One q tile a CTA: two softmax warps per lane quarter (a CTA would otherwise have one
-// softmax warp per SM sub-partition); two q tiles already alternate on the tensor cores.
+// Two softmax warps per lane quarter, halving each warp's per-tile softmax chain: for one
+// q tile a CTA (which would otherwise have one softmax warp per SM sub-partition), and for
+// two where the registers allow (no score features, 16-bit caches: 608 threads).
 template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
 cudaError_t launch_prefill_tm_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
-  constexpr int SW = NQ == 1 ? 2 : 1;
+  constexpr int SW = (NQ == 1 || (!FEAT && !F8)) ? 2 : 1;
   using C = PrefillTmCfg<D, NQ, F8, SW>;
   auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT, F8, SW>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
