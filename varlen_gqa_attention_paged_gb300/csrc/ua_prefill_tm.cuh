@@ -746,12 +746,13 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// Two softmax warps per lane quarter, halving each warp's per-tile softmax chain: for one
-// q tile a CTA (which would otherwise have one softmax warp per SM sub-partition), and for
-// two where the registers allow (no score features, 16-bit caches: 608 threads).
+// One q tile a CTA: two softmax warps per lane quarter (a CTA would otherwise have one
+// softmax warp per SM sub-partition).  Two q tiles already alternate on the tensor cores;
+// splitting their softmax too measured slower on GB300 (the d128 long prefill went from
+// 1.12 to 1.19 ms).
 template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
 cudaError_t launch_prefill_tm_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
-  constexpr int SW = (NQ == 1 || (!FEAT && !F8)) ? 2 : 1;
+  constexpr int SW = NQ == 1 ? 2 : 1;
   using C = PrefillTmCfg<D, NQ, F8, SW>;
   auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT, F8, SW>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
