@@ -402,6 +402,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Approximate reciprocal (one special-function instruction; rcp(+inf) = 0).
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

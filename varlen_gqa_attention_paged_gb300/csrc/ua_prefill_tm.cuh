@@ -246,8 +246,9 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       mbar_arrive_expect_tx(q_full, nq_act * C::kCB * TQ * G * 128);
       for (int qt = 0; qt < nq_act; ++qt)
         for (int cb = 0; cb < C::kCB; ++cb)
-          tma_load_3d_pf(sQ + qt * C::kQBytes + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G,
-                         q0 + t_first + qt * TQ, q_full);
+          tma_load_3d_pf(sQ + qt * C::kQBytes + cb * C::kBM * 128, &pp.tmap_q, 64 * cb,
+                         pp.q_head_major ? q0 + t_first + qt * TQ : g * G,
+                         pp.q_head_major ? g * G : q0 + t_first + qt * TQ, q_full);
     }
     // block id of this lane's 16-key page of key tile j (lanes 0 .. BN/16-1; -1: none)
     auto page_blk = [&](int j) -> int {
@@ -485,13 +486,14 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     tile_walk(qt, jb, je);
     const int n_tiles = je - jb;
     const int tf = t_first + qt * TQ;
-    const int tl = r / G;                                  // token within the q tile
+    // the row's token within the tile and head within the group (head-major or token-major rows)
+    const int tl = pp.q_head_major ? r % TQ : r / G;
     const bool rv = qt < nq_act && r < TQ * G && tf + tl < q_len && q0 + tf + tl < p.total_q;
     // a warp none of whose rows holds a query row (a q tile's unused rows) only keeps the
     // tile barriers in step: what its rows of P and O hold is never stored
     const bool active = __any_sync(0xffffffffu, rv);
     const int i_q = tf + (rv ? tl : 0);                    // query index within the sequence
-    const int h = g * G + r % G;
+    const int h = g * G + (pp.q_head_major ? r / TQ : r % G);
     const int pos = ctx + i_q;
     const int lo_r = p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
     // warp-uniform bounds of this warp's valid rows, to mask only boundary tiles
@@ -501,7 +503,6 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
       lomax = max(lomax, __shfl_xor_sync(0xffffffffu, lomax, o));
     }
-    const float inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
     float slope = 0.f;
     const float* qq_row = nullptr;
     if constexpr (FEAT) {
@@ -527,11 +528,16 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
 
     // softcap / ALiBi / QQ-bias, then (MASK: a boundary tile) the causal / window /
     // partition mask
-    auto score = [&](float v, int jk, auto mask) -> float {
+    // softcap: sc tanh(s / sc) = sc - 2 sc / (1 + 2^(2 log2(e) s / sc)), the score scale folded
+    // into ksc (one exp2, one reciprocal, one FMA; +-inf exponents give +-sc); ALiBi:
+    // slope (j - ctx) as slope e + abase, abase = slope (first key of the chunk - ctx)
+    const float sc = p.softcap;
+    const float ksc = sc > 0.f ? kq * 2.f * kLog2e / sc : 0.f;
+    auto score = [&](float v, int jk, float abase, int e, auto mask) -> float {
       if constexpr (FEAT) {
-        v *= kq;
-        if (p.softcap > 0.f) v = p.softcap * fast_tanh(v * inv_softcap);
-        v += slope * static_cast<float>(jk - ctx);
+        if (sc > 0.f) v = fmaf(-2.f * sc, fast_rcp(fast_exp2(v * ksc) + 1.f), sc);
+        else v *= kq;
+        v += fmaf(slope, static_cast<float>(e), abase);
         if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
       }
       if constexpr (decltype(mask)::value) {
@@ -563,17 +569,18 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
         tmem_ld32(tS + c0 + 32, rb);
         tmem_ld_wait();
         if (rewrite) {
+          const float ab = FEAT ? slope * static_cast<float>(k0 + c0 - ctx) : 0.f;
           if (need_mask) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, std::true_type{}));
-              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::true_type{}));
+              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, ab, e, std::true_type{}));
+              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::true_type{}));
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, std::false_type{}));
-              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::false_type{}));
+              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, ab, e, std::false_type{}));
+              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::false_type{}));
             }
           }
           tmem_st32(tS + c0, ra);

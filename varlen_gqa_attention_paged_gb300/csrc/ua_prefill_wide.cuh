@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
     if (pw == 0 && lane == 0) {
       mbar_arrive_expect_tx(q_full, C::kCB * TQ * G * 128);
       for (int cb = 0; cb < C::kCB; ++cb)
-        tma_load_3d_pf(sQ + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G, q0 + t_first, q_full);
+        tma_load_3d_pf(sQ + cb * C::kBM * 128, &pp.tmap_q, 64 * cb,
+                       pp.q_head_major ? q0 + t_first : g * G, pp.q_head_major ? g * G : q0 + t_first,
+                       q_full);
     }
     const int n_items = 4 * nt;
     // item u: K or V, tile j, half h
@@ -459,10 +461,11 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
   } else {
     // ======================================================== softmax warps (thread = row)
     const int r = 32 * warp + lane;
-    const int tl = r / G;
-    const bool rv = r < (t_last - t_first + 1) * G && q0 + t_first + tl < p.total_q;
+    // the row's token within the tile and head within the group (head-major or token-major rows)
+    const int tl = pp.q_head_major ? r % TQ : r / G;
+    const bool rv = r < TQ * G && tl <= t_last - t_first && q0 + t_first + tl < p.total_q;
     const int i_q = t_first + (rv ? tl : 0);
-    const int h = g * G + r % G;
+    const int h = g * G + (pp.q_head_major ? r / TQ : r % G);
     const int pos = ctx + i_q;
     const int lo_r = p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
     int pmin = rv ? pos : INT_MAX, lomax = rv ? lo_r : INT_MIN;
@@ -471,7 +474,6 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
       pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
       lomax = max(lomax, __shfl_xor_sync(0xffffffffu, lomax, o));
     }
-    const float inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
     float slope = 0.f;
     const float* qq_row = nullptr;
     if constexpr (FEAT) {
@@ -492,11 +494,16 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
     const uint32_t tOr = tO + lane_off;
     bool ok = true;
 
-    auto score = [&](float v, int jk, auto mask) -> float {
+    // softcap: sc tanh(s / sc) = sc - 2 sc / (1 + 2^(2 log2(e) s / sc)), the score scale folded
+    // into ksc (one exp2, one reciprocal, one FMA; +-inf exponents give +-sc); ALiBi:
+    // slope (j - ctx) as slope e + abase, abase = slope (first key of the chunk - ctx)
+    const float sc = p.softcap;
+    const float ksc = sc > 0.f ? kq * 2.f * kLog2e / sc : 0.f;
+    auto score = [&](float v, int jk, float abase, int e, auto mask) -> float {
       if constexpr (FEAT) {
-        v *= kq;
-        if (p.softcap > 0.f) v = p.softcap * fast_tanh(v * inv_softcap);
-        v += slope * static_cast<float>(jk - ctx);
+        if (sc > 0.f) v = fmaf(-2.f * sc, fast_rcp(fast_exp2(v * ksc) + 1.f), sc);
+        else v *= kq;
+        v += fmaf(slope, static_cast<float>(e), abase);
         if (qq_row != nullptr && jk >= ctx && jk <= pos) v += __ldg(qq_row + (jk - ctx));
       }
       if constexpr (decltype(mask)::value) {
@@ -523,17 +530,18 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
         tmem_ld32(tS + c0 + 32, rb);
         tmem_ld_wait();
         if (rewrite) {
+          const float ab = FEAT ? slope * static_cast<float>(k0 + c0 - ctx) : 0.f;
           if (need_mask) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, std::true_type{}));
-              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::true_type{}));
+              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, ab, e, std::true_type{}));
+              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::true_type{}));
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, std::false_type{}));
-              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, std::false_type{}));
+              ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, ab, e, std::false_type{}));
+              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::false_type{}));
             }
           }
           tmem_st32(tS + c0, ra);
