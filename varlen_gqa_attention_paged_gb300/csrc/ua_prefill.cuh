@@ -41,16 +41,37 @@ __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, pf_wait(bar, parity, abort_flag, status));
 }
 
-// Sequence owning token-block slot x: the last b with floor(cu[b] / TQ) + b <= x.
-__device__ __forceinline__ int pf_find_seq(const int32_t* __restrict__ cu, int num_seqs, int x,
-                                           int tq) {
-  int lo = 0, hi = num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(cu + mid) / tq + mid <= x) lo = mid;
-    else hi = mid - 1;
+// Sequence owning token-block slot x and its sizes, found by each warp on its own: lane i
+// reads cu_seqlens_q[i], cu_seqlens_q[i + 1] and seq_lens_k[i] (32 sequences a round, the
+// loads independent and coalesced), the owner is the last b with
+// floor(cu[b] / tb) + b <= x (a ballot; the left side grows strictly with b), and its
+// sizes reach every lane by shuffles.  One round of loads instead of the binary search's
+// chain of dependent ones.
+struct PfSeq {
+  int b, q0, q_len, kv_len;
+};
+__device__ __forceinline__ PfSeq pf_seq_of_slot(const int32_t* __restrict__ cu,
+                                                const int32_t* __restrict__ kvl, int num_seqs,
+                                                int x, int tb) {
+  const int lane = threadIdx.x & 31;
+  PfSeq r{0, 0, 0, 0};
+  for (int base = 0; base < num_seqs; base += 32) {
+    const int i = base + lane;
+    const bool in = i < num_seqs;
+    const int c0 = in ? __ldg(cu + i) : 0;
+    const int c1 = in ? __ldg(cu + i + 1) : 0;
+    const int kv = in ? __ldg(kvl + i) : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, in && c0 / tb + i <= x);
+    if (m != 0u) {
+      const int src = 31 - __clz(m);
+      r.b = base + src;
+      r.q0 = __shfl_sync(0xffffffffu, c0, src);
+      r.q_len = __shfl_sync(0xffffffffu, c1, src) - r.q0;
+      r.kv_len = __shfl_sync(0xffffffffu, kv, src);
+    }
+    if (m != 0xffffffffu) break;  // the owner lies in this round
   }
-  return lo;
+  return r;
 }
 
 }  // namespace ua

@@ -67,7 +67,7 @@ struct PrefillTmCfg {
   static constexpr int kDeqWarps = F8 ? 4 : 0;
   // SW > 1: each tile's row maxima of the SW warps of a row, exchanged through shared
   // memory as bf16 values rounded up
-  static constexpr int kXchBytes = SW > 1 ? NQ * SW * 128 * 2 : 0;
+  static constexpr int kXchBytes = SW > 1 ? NQ * SW * 2 * 128 * 2 : 0;  // two tiles in flight
   // K and V ring depths: as many tiles as fit beside Q (K gets the odd one, at most 4 each)
   static constexpr int kSlots =
       (227 * 1024 - 1024 - kBarBytes - NQ * kQBytes - kF8Bytes - kXchBytes) / kTileBytes;
@@ -97,8 +97,6 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   constexpr int kMma = C::kSoftmaxWarps + 2;
   constexpr int kDeq0 = C::kSoftmaxWarps + 3;  // fp8: dequant warps kDeq0 .. kDeq0 + 3
   const AttnParams& p = pp.p;
-  grid_dependency_wait();
-  grid_launch_dependents();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
@@ -121,17 +119,21 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   uint64_t* const k8_empty = q_ready + 2;
   uint64_t* const v8_full = q_ready + 3;
   uint64_t* const v8_empty = q_ready + 4;
-  uint64_t* const tile_bars = v_empty + RV + (F8 ? 5 : 0);  // [NQ][3]: s_full, p_full, pv_done
+  // [NQ][3]: s_full, p_full, pv_done; then (one q tile: S double-buffered) s_full and
+  // p_full of the second S buffer
+  uint64_t* const tile_bars = v_empty + RV + (F8 ? 5 : 0);
   auto s_full = [&](int qt) { return tile_bars + 3 * qt; };
   auto p_full = [&](int qt) { return tile_bars + 3 * qt + 1; };
   auto pv_done = [&](int qt) { return tile_bars + 3 * qt + 2; };
-  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(tile_bars + 3 * NQ);
+  auto s_full_b = [&](int buf) { return buf ? tile_bars + 3 * NQ : s_full(0); };
+  auto p_full_b = [&](int buf) { return buf ? tile_bars + 3 * NQ + 1 : p_full(0); };
+  uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(tile_bars + 3 * NQ + 2);
   // [NQ][2]: walk step + 1 of the tile's P when its low part matters
   int* const lo_flag = reinterpret_cast<int*>(tmem_holder + 1);
   // SW > 1: per (q tile, lane quarter) a barrier for the tile's row-max exchange and one for
   // the final row-sum exchange ([NQ][4][2]), and the exchanged maxima
   uint64_t* const xch_bars = reinterpret_cast<uint64_t*>(lo_flag + 2 * NQ + 1);  // 8-byte aligned
-  uint16_t* const xch = reinterpret_cast<uint16_t*>(bars) + C::kBarBytes / 2;  // [NQ][SW][128]
+  uint16_t* const xch = reinterpret_cast<uint16_t*>(bars) + C::kBarBytes / 2;  // [NQ][2][SW][128]
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
@@ -141,38 +143,6 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   const int G = p.group;
   const int TQ = pp.tq;          // tokens of one q tile
   const int TB = NQ * TQ;        // tokens of the CTA's q-block
-
-  // Longest walks first: slots are taken in reverse order.
-  const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
-  const int b = pf_find_seq(p.cu_seqlens_q, p.num_seqs, x, TB);
-  const int q0 = __ldg(p.cu_seqlens_q + b);
-  const int q_len = __ldg(p.cu_seqlens_q + b + 1) - q0;
-  const int kv_len = __ldg(p.seq_lens_k + b);
-  const int t_first = (x - (q0 / TB + b)) * TB;  // first token of the block within the sequence
-  if (t_first < 0 || t_first >= q_len) return;   // idle slot: uniform for the CTA
-  const int nq_act = min(NQ, (q_len - t_first + TQ - 1) / TQ);  // q tiles holding tokens
-  const int ctx = kv_len - q_len;
-  // The CTA's key range: the union of its tiles' ranges, split into n_part partitions.
-  const int pos_first = ctx + t_first, pos_last = ctx + min(t_first + TB, q_len) - 1;
-  const int hi = max(0, min(pos_last + 1, kv_len));
-  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
-  int part = (hi - lo + p.n_part - 1) / p.n_part;
-  part = (part + 15) & ~15;
-  const int ks = min(lo + z * part, hi);
-  const int ke = min(ks + part, hi);
-  const int nt = (ke - ks + BN - 1) / BN;
-  // Key tiles [jb, je) of q tile qt: those its own tokens attend to.
-  auto tile_walk = [&](int qt, int& jb, int& je) {
-    jb = je = 0;
-    if (qt >= nq_act) return;
-    const int tf = t_first + qt * TQ, tl = min(tf + TQ, q_len) - 1;
-    const int a = max(ks, p.window_left >= 0 ? max(0, ctx + tf - p.window_left) : 0);
-    const int e = min(ke, max(0, min(ctx + tl + 1, kv_len)));
-    if (a < e) {
-      jb = (a - ks) / BN;
-      je = (e - ks + BN - 1) / BN;
-    }
-  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -195,6 +165,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     }
     if constexpr (SW > 1)
       for (int i = 0; i < NQ * 4 * 2; ++i) mbar_init(&xch_bars[i], 32 * SW);
+    mbar_init(s_full_b(1), 1);
+    mbar_init(p_full_b(1), 4 * SW);
     for (int qt = 0; qt < NQ; ++qt) {
       mbar_init(s_full(qt), 1);
       mbar_init(p_full(qt), 4 * SW);
@@ -223,6 +195,44 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   volatile int* abort_flag = &s_abort;
+  // Everything above touches only this CTA's shared and tensor memory, so it overlaps the
+  // previous kernel's tail (programmatic dependent launch); global memory is read below.
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  // Longest walks first: slots are taken in reverse order.
+  const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  const PfSeq sq = pf_seq_of_slot(p.cu_seqlens_q, p.seq_lens_k, p.num_seqs, x, TB);
+  const int b = sq.b, q0 = sq.q0, q_len = sq.q_len, kv_len = sq.kv_len;
+  const int t_first = (x - (q0 / TB + b)) * TB;  // first token of the block within the sequence
+  if (t_first < 0 || t_first >= q_len) {  // idle slot: uniform for the CTA
+    if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
+    return;
+  }
+  const int nq_act = min(NQ, (q_len - t_first + TQ - 1) / TQ);  // q tiles holding tokens
+  const int ctx = kv_len - q_len;
+  // The CTA's key range: the union of its tiles' ranges, split into n_part partitions.
+  const int pos_first = ctx + t_first, pos_last = ctx + min(t_first + TB, q_len) - 1;
+  const int hi = max(0, min(pos_last + 1, kv_len));
+  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
+  int part = (hi - lo + p.n_part - 1) / p.n_part;
+  part = (part + 15) & ~15;
+  const int ks = min(lo + z * part, hi);
+  const int ke = min(ks + part, hi);
+  const int nt = (ke - ks + BN - 1) / BN;
+  // Key tiles [jb, je) of q tile qt: those its own tokens attend to.
+  auto tile_walk = [&](int qt, int& jb, int& je) {
+    jb = je = 0;
+    if (qt >= nq_act) return;
+    const int tf = t_first + qt * TQ, tl = min(tf + TQ, q_len) - 1;
+    const int a = max(ks, p.window_left >= 0 ? max(0, ctx + tf - p.window_left) : 0);
+    const int e = min(ke, max(0, min(ctx + tl + 1, kv_len)));
+    if (a < e) {
+      jb = (a - ks) / BN;
+      je = (e - ks + BN - 1) / BN;
+    }
+  };
+
 
   if (warp == kProducerK || warp == kProducerV) {
     // ======================================================== TMA producers (K, then V)
@@ -299,7 +309,67 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
 #pragma unroll
     for (int qt = 0; qt < NQ; ++qt) tile_walk(qt, jb[qt], je[qt]);
     bool ok = pf_wait_warp(F8 ? q_ready : q_full, 0, abort_flag, p.status);
-    for (int j = 0; ok && j <= nt; ++j) {
+    if constexpr (NQ == 1) {
+      // One q tile: S double-buffered in tensor memory (columns 0 and BN; O from 2 BN), so
+      // the tensor cores compute S_{j+1} while the softmax works on S_j.  Issue order
+      // S_0, S_1, then for every j: [P_j ready] P.V_j, S_{j+2}; S_{j+2} overwrites P_j
+      // only after P.V_j read it (tensor-core operations of one thread run in order).  One
+      // pv_done phase per P.V.
+      auto qk = [&](int j) -> bool {
+        if (!pf_wait_warp(&k_full[j % RK], (j / RK) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t qb = smem_addr(sQ);
+        const uint32_t kb = smem_addr(sK + (j % RK) * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(qb + (kk >> 2) * C::kBM * 128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kKVCB + (kk & 3) * 32, 16, 1024);
+          umma_f16_ss_warp(tmem + (j & 1) * BN, ad, bd, kIdQK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit_warp(s_full_b(j & 1));
+        umma_commit_warp(&k_empty[j % RK]);
+        return true;
+      };
+      auto pv = [&](int j) -> bool {
+        if (!pf_wait_warp(p_full_b(j & 1), (j >> 1) & 1, abort_flag, p.status)) return false;
+        if (!pf_wait_warp(&v_full[j % RV], (j / RV) & 1, abort_flag, p.status)) return false;
+        uint8_t* vs = sV + (j % RV) * C::kTileBytes;
+        const int k0 = ks + j * BN;
+        if (!F8 && k0 + BN > kv_len) {  // NaN hygiene, as below
+          const int r_lo = max(0, kv_len - k0), r_hi = min(BN, ((kv_len + 15) & ~15) - k0);
+          for (int e = lane; e < (r_hi - r_lo) * C::kCB * 8; e += 32) {
+            const int r = r_lo + e / (C::kCB * 8), c = e % (C::kCB * 8);
+            *reinterpret_cast<uint4*>(vs + (c / 8) * C::kKVCB + r * 128 + (c % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_after();
+        const bool use_lo = BF16 && lo_flag[j & 1] == j + 1;
+        const uint32_t tP = tmem + (j & 1) * BN;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          if (part == 1 && !use_lo) break;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(smem_addr(vs) + kk * 16 * 128, C::kKVCB, 1024);
+            umma_f16_ts_warp(tmem + 2 * BN, tP + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bd,
+                             kIdPV, (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit_warp(pv_done(0));
+        umma_commit_warp(&v_empty[j % RV]);
+        return true;
+      };
+      if (ok && nt > 0) ok = qk(0);
+      if (ok && nt > 1) ok = qk(1);
+      for (int j = 0; ok && j < nt; ++j) {
+        ok = pv(j);
+        if (ok && j + 2 < nt) ok = qk(j + 2);
+      }
+    }
+    for (int j = 0; NQ > 1 && ok && j <= nt; ++j) {
       const int i = j - 1;  // key tile of this step's P.V
       uint8_t* vs = sV + (i >= 0 ? i % RV : 0) * C::kTileBytes;
       if (i >= 0) {
@@ -481,7 +551,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     const int half = (warp % (4 * SW)) >> 2;               // its column slice
     const int r = 32 * quad + lane;                        // row within the q tile
     uint64_t* const xbar = xch_bars + 2 * (4 * qt + quad);  // [0]: row max, [1]: row sum
-    uint16_t* const xrow = xch + (qt * SW) * 128 + r;       // + h * 128
+    uint16_t* const xrow = xch + (qt * 2 * SW) * 128 + r;   // + (slot * SW + h) * 128
     int jb, je;
     tile_walk(qt, jb, je);
     const int n_tiles = je - jb;
@@ -522,8 +592,11 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     const bool sink = p.sinks != nullptr && z == 0 && rv;
     float m_used = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
     float l = sink && half == 0 ? 1.f : 0.f;  // the sink's share, counted once per row
-    const uint32_t tS = tmem + qt * C::kTmemStride + ((32u * quad) << 16);
-    const uint32_t tO = tS + BN;
+    // one q tile: S buffers at columns 0 and BN, O at 2 BN; two: tile qt's S then O
+    constexpr bool DB = NQ == 1;
+    const uint32_t lane_off = (32u * quad) << 16;
+    const uint32_t tS0 = tmem + (DB ? 0u : static_cast<uint32_t>(qt * C::kTmemStride)) + lane_off;
+    const uint32_t tO = DB ? tmem + 2 * BN + lane_off : tS0 + BN;
     bool ok = true;
 
     // softcap / ALiBi / QQ-bias, then (MASK: a boundary tile) the causal / window /
@@ -547,12 +620,15 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     };
 
     for (int n = 0; n < n_tiles; ++n) {
-      if (!pf_wait_warp(s_full(qt), n & 1, abort_flag, p.status)) { ok = false; break; }
+      uint64_t* const sf = DB ? s_full_b(n & 1) : s_full(qt);
+      uint64_t* const pf = DB ? p_full_b(n & 1) : p_full(qt);
+      const uint32_t tS = DB ? tS0 + (n & 1) * BN : tS0;
+      if (!pf_wait_warp(sf, DB ? (n >> 1) & 1 : n & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       if (!active) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(qt));
+        if (lane == 0) mbar_arrive(pf);
         continue;
       }
       const int k0 = ks + (jb + n) * BN;
@@ -595,18 +671,19 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       if (rewrite) tmem_st_wait();
       float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
       if constexpr (SW > 1) {
-        // the row's other column slices: every lane arrives once its value is written.  The
-        // buffer is rewritten for tile n + 1 only after every warp's P of tile n (its S
-        // wait follows the P.V that waited for them), so one buffer serves every tile.
+        // the row's other column slices: every lane arrives once its value is written.  Two
+        // slots: a warp writes tile n + 2's slot only after its S wait, which follows the
+        // P.V of tile n, which waited for every warp's P of tile n, written after the reads.
         const uint32_t u = __float_as_uint(mx);
-        xrow[half * 128] = static_cast<uint16_t>(
+        uint16_t* const slot = xrow + (n & 1) * SW * 128;
+        slot[half * 128] = static_cast<uint16_t>(
             ((u & 0xFFFFu) == 0u || (u >> 31)) ? (u >> 16) : (u >> 16) + 1u);  // round up
         mbar_arrive(&xbar[0]);
         if (!pf_wait_warp(&xbar[0], n & 1, abort_flag, p.status)) { ok = false; break; }
         mx = -INFINITY;
 #pragma unroll
         for (int hh = 0; hh < SW; ++hh)
-          mx = fmaxf(mx, __uint_as_float(static_cast<uint32_t>(xrow[hh * 128]) << 16));
+          mx = fmaxf(mx, __uint_as_float(static_cast<uint32_t>(slot[hh * 128]) << 16));
       }
       // ---- running max, used lazily: O and l are rescaled only when the max grows by
       // more than 8 in log2 units (P stays <= 256, far inside the fp32 and P ranges)
@@ -617,7 +694,13 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
         m_used = mx;
       }
       const float m_use = m_used == -INFINITY ? 0.f : m_used;
-      // O holds P.V of step n-1 (its commit preceded this step's S): rescale it in place
+      // O holds P.V of step n-1: with one S buffer the commit of this step's S covered it;
+      // with two (S_n issued before P.V_{n-1}) wait for that P.V's own phase, every step,
+      // so the parity waits stay exact
+      if (DB && n >= 1) {
+        if (!pf_wait_warp(pv_done(0), (n - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+      }
       if (n >= 1 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
         for (int c0 = half * kOCols; c0 < (half + 1) * kOCols; c0 += 32) {
@@ -676,22 +759,24 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       if (warp_lo && lane == 0) lo_flag[2 * qt + (n & 1)] = n + 1;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(qt));
+      if (lane == 0) mbar_arrive(pf);
     }
 
     // ---- epilogue: O / l for one partition, or the partition's max / sum / O
-    if (ok && n_tiles > 0) ok = pf_wait_warp(pv_done(qt), 0, abort_flag, p.status);
+    // the last P.V (two S buffers: the tile's last pv_done phase; one: its only phase)
+    if (ok && n_tiles > 0 && active)
+      ok = pf_wait_warp(pv_done(qt), DB ? (n_tiles - 1) & 1 : 0, abort_flag, p.status);
     tc_fence_after();
     if constexpr (SW > 1) {
       if (ok && active) {  // the row sum over every column slice, through tensor memory
-        tmem_st1(tS + half, __float_as_uint(l));
+        tmem_st1(tS0 + half, __float_as_uint(l));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&xbar[1]);
         ok = pf_wait_warp(&xbar[1], 0, abort_flag, p.status);
         tc_fence_after();
         uint32_t l0, l1;
-        tmem_ld2(tS, l0, l1);
+        tmem_ld2(tS0, l0, l1);
         tmem_ld_wait();
         l = __uint_as_float(l0) + __uint_as_float(l1);
       }

@@ -130,10 +130,8 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
 
   // Longest walks first: slots are taken in reverse order.
   const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
-  const int b = pf_find_seq(p.cu_seqlens_q, p.num_seqs, x, TQ);
-  const int q0 = __ldg(p.cu_seqlens_q + b);
-  const int q_len = __ldg(p.cu_seqlens_q + b + 1) - q0;
-  const int kv_len = __ldg(p.seq_lens_k + b);
+  const PfSeq sq = pf_seq_of_slot(p.cu_seqlens_q, p.seq_lens_k, p.num_seqs, x, TQ);
+  const int b = sq.b, q0 = sq.q0, q_len = sq.q_len, kv_len = sq.kv_len;
   const int t_first = (x - (q0 / TQ + b)) * TQ;
   if (t_first < 0 || t_first >= q_len) return;   // idle slot: uniform for the CTA
   const int t_last = min(t_first + TQ, q_len) - 1;
