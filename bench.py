@@ -476,7 +476,7 @@ def run_ours(args):
 
     # end-to-end through the public API with host buffers: each step's inputs travel from
     # pinned host memory and its output comes back, all inside the timed region
-    e2e_steps = max(10, min(args.steps, 500))
+    e2e_steps = max(200, min(args.steps, 1000))
     e2e_ms, h2d, d2h = e2e_pipelined(inp, call, dev, stream, reps, e2e_steps)
     clocks = sampler.stop() if rank == 0 else None
 

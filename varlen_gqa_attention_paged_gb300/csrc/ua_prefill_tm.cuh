@@ -638,28 +638,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       // or a mask get it here, once, and are written back over S for pass 2.
       const bool rewrite = FEAT || need_mask;
       float mx0 = -INFINITY, mx1 = -INFINITY;
-      // Two q tiles and no score features: the row's 128 scores stay in registers from pass 1
-      // to pass 2 (one tensor-memory read of S a tile instead of two).
-      constexpr bool KEEP = !FEAT && !F8 && SW == 1 && NQ == 2;
-      uint32_t sv[KEEP ? BN : 1];
-      if constexpr (KEEP) {
-#pragma unroll
-        for (int q = 0; q < BN / 32; ++q)
-          tmem_ld32(tS + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q));
-        tmem_ld_wait();
-        if (need_mask) {
-#pragma unroll
-          for (int e = 0; e < BN; ++e)
-            sv[e] = __float_as_uint(score(__uint_as_float(sv[e]), k0 + e, 0.f, e, std::true_type{}));
-        }
-#pragma unroll
-        for (int e = 0; e < BN; e += 4) {
-          mx0 = fmax3(mx0, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
-        }
-      }
 #pragma unroll 1
-      for (int c0 = half * kCols; !KEEP && c0 < (half + 1) * kCols; c0 += 64) {
+      for (int c0 = half * kCols; c0 < (half + 1) * kCols; c0 += 64) {
         uint32_t ra[32], rb[32];
         tmem_ld32(tS + c0, ra);
         tmem_ld32(tS + c0 + 32, rb);
@@ -688,7 +668,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
           mx1 = fmax3(mx1, __uint_as_float(rb[e]), __uint_as_float(rb[e + 1]));
         }
       }
-      if (rewrite && !KEEP) tmem_st_wait();
+      if (rewrite) tmem_st_wait();
       float mx = fmaxf(mx0, mx1) * c;  // row max in log2 units (-inf stays -inf)
       if constexpr (SW > 1) {
         // the row's other column slices: every lane arrives once its value is written.  Two
@@ -771,17 +751,12 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
         }
         tmem_st32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(rr));
       };
-      if constexpr (KEEP) {
-#pragma unroll
-        for (int q = 0; q < BN / 32; ++q) p_group(32 * q, sv + 32 * q);
-      } else {
 #pragma unroll 1
-        for (int c0 = half * kCols; c0 < (half + 1) * kCols; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tS + c0, rr);
-          tmem_ld_wait();
-          p_group(c0, rr);
-        }
+      for (int c0 = half * kCols; c0 < (half + 1) * kCols; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tS + c0, rr);
+        tmem_ld_wait();
+        p_group(c0, rr);
       }
       l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
       tmem_st_wait();
