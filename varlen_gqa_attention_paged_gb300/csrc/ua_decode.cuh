@@ -153,6 +153,17 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
     const uint64_t policy = l2_policy_evict_first();
     const int bs = p.block_size;
     const int oob = p.num_blocks * bs;
+    auto page_row = [&](int t) -> int {
+      const int key = ks + t * T + 16 * lane;
+      if (lane >= T / 16 || key >= ke) return oob;
+      const int col = key / bs;
+      const int blk = col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
+      if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+        atomicOr(p.status, DEV_BAD_BLOCK);
+        return oob;
+      }
+      return blk * bs + key % bs;
+    };
     // Per-token scales of this lane's kKPL keys kKPL lane .. of tile t (one page; 0 past
     // the walk): the page's block id is loaded two tiles ahead, the scales one tile ahead.
     constexpr int KPL = C::kKPL;
@@ -184,33 +195,12 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
       if (ntiles > 0) load_scales(0, scale_blk(0), sc_next);
       blk_next = scale_blk(1);
     }
-    // Block ids of this lane's page, loaded four tiles before their use (a register
-    // pipeline), so a stage's copies never wait on a block-table load; the id is checked
-    // and turned into a cache row when used.
-    auto page_blk = [&](int t) -> int {
-      const int key = ks + t * T + 16 * lane;
-      if (t >= ntiles || lane >= T / 16 || key >= ke) return 0;
-      const int col = key / bs;
-      return col < p.max_blocks_per_seq ? __ldg(bt + col) : -1;
-    };
-    auto row_of = [&](int t, int blk) -> int {
-      const int key = ks + t * T + 16 * lane;
-      if (lane >= T / 16 || key >= ke) return oob;
-      if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
-        atomicOr(p.status, DEV_BAD_BLOCK);
-        return oob;
-      }
-      return blk * bs + key % bs;
-    };
-    int blk0 = page_blk(0), blk1 = page_blk(1), blk2 = page_blk(2), blk3 = page_blk(3);
     int issued = 0;
+    int row_next = ntiles > 0 ? page_row(0) : oob;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % S;
-      const int row = row_of(t, blk0);
-      blk0 = blk1;
-      blk1 = blk2;
-      blk2 = blk3;
-      blk3 = page_blk(t + 4);
+      const int row = row_next;
+      if (t + 1 < ntiles) row_next = page_row(t + 1);  // block-table lookups one tile ahead
       float sc_cur[KPL][2];
 #pragma unroll
       for (int e = 0; e < KPL; ++e) {
