@@ -485,10 +485,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
               true, &pl);
     p.n_part = pl.n_part;
   }
-  // per-token fp8 scales: the decode tile reads them (decode batches, head_dim <= 128,
-  // 16 | block_size); other shapes have no kernel for them
   // per-token fp8 scales: the decode tile and the tensor-memory kernels read them (the tile
-  // kernel, for 9 to 16 rows a kv-head or pages not a multiple of 16, does not)
+  // kernel, for decode batches of 9 to 16 rows a kv-head or head_dim 256, and for pages
+  // not a multiple of 16, does not)
   if (tok_scales && pl.kernel != ua::KERNEL_DEC8 && pl.kernel != ua::KERNEL_DEC8W &&
       !is_tc(pl.kernel))
     return UA_ERR_UNSUPPORTED;
