@@ -76,7 +76,7 @@ def kernel_name(plan, head_dim):
     """The attention kernel a plan launches."""
     if plan["kernel"] in (8, 16):
         return "ua_prefill_tm_kernel" if head_dim <= 128 else "ua_prefill_wide_kernel"
-    if plan["kernel"] in (2, 32):
+    if plan["kernel"] in (2, 32, 64):
         return "ua_decode_kernel"
     return "ua_attn_tile_kernel"
 
@@ -210,7 +210,8 @@ class Call:
                             kv_dtype=ua._DTYPES[inp.spec.kv_dtype],
                             q_dtype=ua._DTYPES[inp.spec.q_dtype], backend=backend,
                             max_blocks_per_seq=self.tables[0].shape[-1],
-                            num_blocks=self.d["k_cache"].shape[0])
+                            num_blocks=self.d["k_cache"].shape[0],
+                            per_token_scales=inp.k_scale_tok is not None)
         self.shape = ua._shape(self.d["q"], self.d["k_cache"], self.tables[0],
                                self.d["cu_seqlens_q"], inp.max_seqlen_q, inp.max_seqlen_k,
                                self.d["qq_bias"], ua._DTYPES[self.out.dtype], 0, None, None,

@@ -137,12 +137,15 @@ typedef struct {
                           taken as f16); 16: the same
                           kernel with two such tiles of consecutive tokens per CTA; 32: the
                           key-major decode tile of code 2 with eight consumer warps (128-key
-                          stages, one CTA per SM), for decode grids of at most one CTA per SM */
+                          stages, one CTA per SM), for decode grids of at most one CTA per SM;
+                          64: the decode tile of code 2 with two kv-heads per CTA (fp8 caches
+                          with per-tensor scales, at most 4 rows per kv-head, an even
+                          num_kv_heads): one page box carries both heads' rows */
   int32_t block_m;     /* (query token x head) rows per q-block */
   int32_t n_part;      /* key-range partitions (1 on the 2D path) */
   int32_t grid_x;      /* q-block slots: num_seqs when slot_per_seq, else
                           floor(total_q * G / block_m) + num_seqs */
-  int32_t grid_y;      /* num_kv_heads */
+  int32_t grid_y;      /* num_kv_heads (num_kv_heads / 2 for kernel 64) */
   int32_t grid_z;      /* n_part */
   int32_t num_sms;     /* SM count the plan was made for */
   int32_t cluster_y;   /* CTAs of one q-block slot (different kv-heads) launched as a cluster */

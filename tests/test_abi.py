@@ -161,7 +161,7 @@ def test_dispatcher_split_fits_one_wave():
         p = _plan(num_seqs=seqs, total_q=seqs, num_kv_heads=hkv, num_q_heads=4 * hkv, kv_dtype=kv,
                   window_left=-1, max_seqlen_k=100000)
         active = seqs * p["grid_y"]                     # CTAs of one partition
-        per_sm = 3 if p["kernel"] == 2 else 2           # the decode tile fits three an SM
+        per_sm = 3 if p["kernel"] == 2 else 2  # decode tile: three an SM (two-head tile: two)
         assert p["path"] == _lib.UA_PATH_SPLIT
         assert active * p["n_part"] <= per_sm * 152
         # the largest count that fits: one more partition would start a second wave (of
@@ -172,7 +172,13 @@ def test_dispatcher_split_fits_one_wave():
 def test_dispatcher_decode_kernels():
     # at most 8 rows per kv-head, head_dim <= 128, page boxes: the key-major decode tile
     assert _plan()["kernel"] == 2
-    assert _plan(head_dim=64, kv_dtype=2)["kernel"] == 2
+    # fp8 with at most 4 rows per kv-head and an even kv-head count: two kv-heads a CTA
+    p = _plan(head_dim=64, kv_dtype=2)
+    assert p["kernel"] == 64 and p["grid_y"] == 4 and p["block_m"] == 8
+    assert _plan(kv_dtype=2, max_seqlen_q=2)["kernel"] == 2          # 8 rows a kv-head
+    assert _plan(kv_dtype=2, num_kv_heads=1, num_q_heads=4)["kernel"] in (2, 32)  # one kv-head
+    assert _plan(kv_dtype=2, num_kv_heads=4, num_q_heads=4, max_seqlen_q=4)["kernel"] == 64
+    assert _plan(kv_dtype=2, per_token_scales=True)["kernel"] == 2  # scales: one head a CTA
     # more rows (up to 16), head_dim 256, pages not a multiple of 16: the 16-row tile
     assert _plan(max_seqlen_q=3)["kernel"] == 1
     assert _plan(head_dim=256)["kernel"] == 1

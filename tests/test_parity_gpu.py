@@ -72,7 +72,8 @@ def _plan(inp, backend="auto", num_splits=0):
                    head_dim=spec.head_dim, window_left=inp.window_left,
                    kv_dtype=ua._DTYPES[spec.kv_dtype], q_dtype=ua._DTYPES[spec.q_dtype],
                    backend=backend, num_splits=num_splits, max_blocks_per_seq=bt.shape[-1],
-                   num_blocks=inp.k_cache.shape[0])
+                   num_blocks=inp.k_cache.shape[0],
+                   per_token_scales=inp.k_scale_tok is not None)
 
 
 def _tile_rows(inp, tokens_per_tile, tiles_per_seq=64):
@@ -266,6 +267,20 @@ SMALL = {
     "dec_fp8_tok_d64_bs32": dict(seqs=[(1, 900), (1, 65), (1, 31)], num_q_heads=16,
                                  num_kv_heads=2, head_dim=64, block_size=32,
                                  kv_dtype=torch.float8_e4m3fn, per_token_scales=True),
+    # fp8 decode with at most 4 rows per kv-head: two kv-heads a CTA (one page box carries
+    # both heads' rows; their q-blocks share the tile's 8 columns).  Every score feature,
+    # empty and one-key rows (G 2, q_len 2); columns left empty in each head (G 3), an f16
+    # q (three e4m3 terms of Q); head_dim 64 with one head a group and 4-token chunks
+    "dec_fp8_pair_feat": dict(seqs=[(1, 700), (2, 129), (1, 1), (1, 17), (1, 0), (2, 333)],
+                              num_q_heads=8, num_kv_heads=4, kv_dtype=torch.float8_e4m3fn,
+                              q_dtype=torch.bfloat16, softcap=25.0, alibi=True, qq_bias=True,
+                              qq_bias_shape=(8, 16), sinks=True, window=260),
+    "dec_fp8_pair_g3_f16q": dict(seqs=[(1, 900), (1, 65), (1, 31), (1, 200)], num_q_heads=12,
+                                 num_kv_heads=4, block_size=32, kv_dtype=torch.float8_e4m3fn,
+                                 sinks=True),
+    "dec_fp8_pair_d64_mha": dict(seqs=[(4, 500), (1, 64), (3, 129)], num_q_heads=6,
+                                 num_kv_heads=6, head_dim=64, q_dtype=torch.bfloat16,
+                                 kv_dtype=torch.float8_e4m3fn, window=100, sinks=True),
     # 9 to 16 rows per kv-head, and head_dim 256: the 16-row tile kernel's decode path
     "tile16_bf16_g8_q2": dict(seqs=[(2, 700), (1, 300), (2, 45), (1, 1)], num_q_heads=16,
                               num_kv_heads=2, q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16,
@@ -465,6 +480,21 @@ def test_both_decode_tile_widths_run():
     assert _plan(inp, "2d")["kernel"] == 32
     want = oracle.attention(threads=THREADS, **inp.oracle_kwargs())
     assert max_err(run(inp, backend="2d"), want) <= TOL[spec.kv_dtype]
+
+
+def test_two_kv_heads_per_decode_tile():
+    """fp8 decode batches of at most 4 rows per kv-head (an even kv-head count, per-tensor
+    scales) run two kv-heads a CTA: the sliding-window fp8 decode and the pair cases above;
+    8 rows a kv-head, or per-token scales, keep one head a CTA."""
+    assert _plan(inputs(W.SWDECODE_FP8))["kernel"] == 64
+    assert _plan(inputs(W.SWDECODE_FP8_TOK))["kernel"] == 2
+    for case in ("dec_fp8_pair_feat", "dec_fp8_pair_g3_f16q", "dec_fp8_pair_d64_mha"):
+        spec = _small(100 + sorted(SMALL).index(case), **SMALL[case])
+        inp = W.make(spec, poison=True)
+        for backend in ("auto", "2d", "split"):
+            assert _plan(inp, backend)["kernel"] == 64, (case, backend)
+    spec = _small(100 + sorted(SMALL).index("dec_fp8_feat"), **SMALL["dec_fp8_feat"])
+    assert _plan(W.make(spec), "2d")["kernel"] in (2, 32)
 
 
 def test_out_of_range_block_id_is_reported_not_read():

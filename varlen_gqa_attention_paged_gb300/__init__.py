@@ -218,10 +218,15 @@ def prepare(q, k_cache, v_cache, cu_seqlens_q, seq_lens_k, block_table, *, max_s
 
 def plan(*, num_seqs, total_q, max_seqlen_q, max_seqlen_k, block_size, num_q_heads,
          num_kv_heads, head_dim, window_left=-1, kv_dtype=UA_DT_BF16, q_dtype=None,
-         backend="auto", num_splits=0, num_sms=0, max_blocks_per_seq=1, num_blocks=1):
-    """The dispatcher's decision for these sizes (host only; no GPU needed when num_sms > 0)."""
+         backend="auto", num_splits=0, num_sms=0, max_blocks_per_seq=1, num_blocks=1,
+         per_token_scales=False):
+    """The dispatcher's decision for these sizes (host only; no GPU needed when num_sms > 0).
+    per_token_scales: plan for an fp8 call with per-token K/V scales (the dispatcher only
+    tests the scale pointers for null; this passes a placeholder that is never read)."""
     lib = _lib.load()
     sh = _lib.UaShape()
+    if per_token_scales:
+        sh.k_scale_tok = sh.v_scale_tok = 256
     sh.num_seqs, sh.total_q = num_seqs, total_q
     sh.max_seqlen_q, sh.max_seqlen_k = max_seqlen_q, max_seqlen_k
     sh.max_blocks_per_seq, sh.num_blocks = max_blocks_per_seq, num_blocks

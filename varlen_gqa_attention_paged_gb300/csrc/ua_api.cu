@@ -134,10 +134,12 @@ bool encode_q_map(CUtensorMap* map, const void* q, int q_dtype, int total_q, int
 
 // A paged cache [num_blocks * block_size][H_kv][D] as a 3-D TMA tensor; one box is 16
 // cache rows of one kv-head and one column block (128 bytes, swizzled; 64-byte rows
-// unswizzled).  Rows past the tensor read as zero.
+// unswizzled).  Rows past the tensor read as zero.  With heads_per_box > 1 the view is
+// [H_kv][rows][D] (head outermost) and a box is 16 rows of heads_per_box consecutive
+// kv-heads, landing head by head.
 bool encode_cache_map(CUtensorMap* map, const void* base, int kv_dtype, int num_blocks,
-                      int block_size, int hkv, int d) {
-  const MapKey key{base, 1, kv_dtype, d, hkv, num_blocks, block_size, 0};
+                      int block_size, int hkv, int d, int heads_per_box = 1) {
+  const MapKey key{base, 1, kv_dtype, d, hkv, num_blocks, block_size, heads_per_box};
   if (map_cache().find(key, map)) return true;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
@@ -147,11 +149,18 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int kv_dtype, int num_
   const CUtensorMapDataType dt = kv_dtype == UA_DT_F8E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : kv_dtype == UA_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
-                              static_cast<cuuint64_t>(num_blocks) * block_size};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
-                                 static_cast<cuuint64_t>(row_bytes) * hkv};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(cbw / esz), 1, 16};
+  const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * block_size;
+  const cuuint64_t head_stride = static_cast<cuuint64_t>(row_bytes);
+  const cuuint64_t row_stride = static_cast<cuuint64_t>(row_bytes) * hkv;
+  const bool head_outer = heads_per_box > 1;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d),
+                              head_outer ? rows : static_cast<cuuint64_t>(hkv),
+                              head_outer ? static_cast<cuuint64_t>(hkv) : rows};
+  const cuuint64_t strides[2] = {head_outer ? row_stride : head_stride,
+                                 head_outer ? head_stride : row_stride};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(cbw / esz),
+                             head_outer ? 16u : 1u,
+                             head_outer ? static_cast<cuuint32_t>(heads_per_box) : 16u};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -224,6 +233,11 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
   // decode with at most 8 rows per kv-head: the key-major decode tile (page boxes)
   const bool dec = allow_dec && !tc && rows_max <= 8 && d <= 128 && block_size % 16 == 0 &&
                    static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
+  // fp8 decode with at most 4 rows per kv-head and per-tensor scales: two kv-heads a CTA
+  // (their q-blocks fill the tile's 8 columns; one page box carries both heads' rows)
+  const bool pair = dec && kv_dtype == UA_DT_F8E4M3 && rows_max <= 4 && hkv % 2 == 0 &&
+                    sh->k_scale_tok == nullptr;
+  const int gy = pair ? hkv / 2 : hkv;  // CTAs of one slot (grid y)
   const int wm = dec ? ua::KERNEL_DEC8 : rows_max <= 16 ? 1 : 4;
   const int tq = tc ? 128 / group : 0;               // tokens per 128-row tensor-memory tile
   // two tiles per CTA (sharing every K/V tile) where their tensor memory fits and the
@@ -240,14 +254,17 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
          : per_seq ? sh->num_seqs
                    : static_cast<long long>(sh->total_q) * group / bm + sh->num_seqs;
   const long long active = per_seq ? std::min<long long>(sh->num_seqs, sh->total_q) : slots;
-  const long long base = std::max<long long>(1, active * hkv);
+  const long long base = std::max<long long>(1, active * gy);
   // Longest key walk of one q-block: a window bounds it, otherwise the longest sequence.
   long long walk = sh->max_seqlen_k;
   if (window_left >= 0)
     walk = std::min<long long>(walk, static_cast<long long>(window_left) + 1 + (bm + group - 1) / group);
   const long long wave =
       static_cast<long long>(num_sms) *
-      (tc ? 1 : dec ? ua::decode_ctas_per_sm(d, kv_dtype) : ua::tile_ctas_per_sm(d, kv_dtype, wm));
+      (tc    ? 1
+       : pair ? ua::decode_pair_ctas_per_sm(d)
+       : dec  ? ua::decode_ctas_per_sm(d, kv_dtype)
+              : ua::tile_ctas_per_sm(d, kv_dtype, wm));
   const long long by_walk = std::max<long long>(1, walk / kMinPartitionKeys);
   const long long fit = std::max<long long>(2, std::min(wave / base, by_walk));
   int n_part = 1;
@@ -271,7 +288,7 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
     cy = 1;
     if (!tc && wm != 4)
       for (int c = 8; c > 1; c >>= 1)
-        if (hkv % c == 0) {
+        if (gy % c == 0) {
           cy = c;
           break;
         }
@@ -292,32 +309,35 @@ void make_plan(const ua_shape_t* sh, int block_size, int hq, int hkv, int d, int
       const int c = cy * cz;
       if (c <= 1) break;
       long long cap = -1;
-      if (dec && query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, false, cy, cz);
+      if (dec && query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, false, pair, cy, cz);
       if (cap < 0) cap = c <= 2 ? wave / c : (wave * 9 / 10) / c;
-      if (slots * (hkv / cy) <= cap) break;
+      if (slots * (gy / cy) <= cap) break;
     }
   }
   // A decode grid of at most one CTA per SM runs the eight-warp decode tile (128-key
   // stages): twice the consumer warps on each CTA's key walk, half the pipeline stages,
   // when its clusters (one CTA per SM) are all resident together.
   bool wide = false;
-  if (dec && slots * hkv * n_part <= num_sms) {
+  if (dec && !pair && slots * hkv * n_part <= num_sms) {
     int cy, cz;
     cluster_shape(n_part, cy, cz);
     wide = true;
     if (cy * cz > 1) {
       long long cap = -1;
-      if (query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, true, cy, cz);
+      if (query_device) cap = ua::decode_cluster_capacity(d, kv_dtype, true, false, cy, cz);
       if (cap < 0) cap = (static_cast<long long>(num_sms) * 9 / 10) / (cy * cz);
       wide = slots * (hkv / cy) <= cap;
     }
   }
   pl->path = n_part > 1 ? UA_PATH_SPLIT : UA_PATH_2D;
-  pl->kernel = tc ? (nq == 2 ? ua::KERNEL_TC256 : ua::KERNEL_TC128) : wide ? ua::KERNEL_DEC8W : wm;
+  pl->kernel = tc     ? (nq == 2 ? ua::KERNEL_TC256 : ua::KERNEL_TC128)
+               : pair ? ua::KERNEL_DEC8P
+               : wide ? ua::KERNEL_DEC8W
+                      : wm;
   pl->block_m = bm;
   pl->n_part = n_part;
   pl->grid_x = static_cast<int32_t>(slots);
-  pl->grid_y = hkv;
+  pl->grid_y = gy;
   pl->grid_z = n_part;
   pl->num_sms = num_sms;
   int cy, cz;
@@ -476,10 +496,14 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   // decode tile needs them, else the call is planned again for the tile kernel.
   bool tma = !is_tc(pl.kernel) && block_size % 16 == 0 &&
              static_cast<long long>(sh->num_blocks) * block_size + 16 <= INT32_MAX;
+  const int hbox = pl.kernel == ua::KERNEL_DEC8P ? 2 : 1;  // kv-heads per page box
   if (tma)
-    tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d) &&
-          encode_cache_map(&tp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d);
-  const bool dec_kernel = pl.kernel == ua::KERNEL_DEC8 || pl.kernel == ua::KERNEL_DEC8W;
+    tma = encode_cache_map(&tp.tmap_k, k_cache, kv_dtype, sh->num_blocks, block_size, hkv, d,
+                           hbox) &&
+          encode_cache_map(&tp.tmap_v, v_cache, kv_dtype, sh->num_blocks, block_size, hkv, d,
+                           hbox);
+  const bool dec_kernel = pl.kernel == ua::KERNEL_DEC8 || pl.kernel == ua::KERNEL_DEC8W ||
+                          pl.kernel == ua::KERNEL_DEC8P;
   if (dec_kernel && !tma) {
     make_plan(sh, block_size, hq, hkv, d, window_left, kv_dtype, backend, num_sms, false, false,
               true, &pl);
@@ -520,6 +544,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, void* out,
   } else if (pl.kernel == ua::KERNEL_DEC8) {
     err = d == 64 ? ua::launch_decode_w4_d64(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st)
                   : ua::launch_decode_w4_d128(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st);
+  } else if (pl.kernel == ua::KERNEL_DEC8P) {
+    err = d == 64 ? ua::launch_decode_pair_d64(tp, grid, feat, pl.cluster_y, pl.cluster_z, st)
+                  : ua::launch_decode_pair_d128(tp, grid, feat, pl.cluster_y, pl.cluster_z, st);
   } else if (pl.kernel == ua::KERNEL_DEC8W) {
     err = d == 64 ? ua::launch_decode_w8_d64(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st)
                   : ua::launch_decode_w8_d128(tp, grid, kv, feat, pl.cluster_y, pl.cluster_z, st);

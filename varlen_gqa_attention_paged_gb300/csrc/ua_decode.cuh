@@ -25,12 +25,15 @@
 namespace ua {
 
 // W consumer warps (4, or 8 for grids of at most one CTA per SM), each taking 16 keys of
-// every stage.
-template <int D, int KV, int W = 4>
+// every stage.  HP kv-heads per CTA (1, or 2 for fp8 caches with at most 4 rows per kv-head:
+// the two heads' q-blocks share the MMA's 8 columns, and one page box carries both heads).
+template <int D, int KV, int W = 4, int HP = 1>
 struct DecCfg {
   static constexpr int kConsumerWarps = W;
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);
   static constexpr int kRows = 8;                  // rows of a q-block (the MMA's N)
+  static constexpr int kHP = HP;
+  static constexpr int kRH = kRows / HP;           // rows of one kv-head (columns kRH h ..)
   static constexpr int kT = 16 * W;                // keys per pipeline stage (W pages of 16)
   static constexpr int kKPL = kT / 32;             // keys whose scales one producer lane stages
   static constexpr int kEsz = KvTraits<KV>::kEsz;
@@ -38,7 +41,7 @@ struct DecCfg {
   static constexpr bool kSwz = kRowBytes >= 128;   // 128-byte swizzled column blocks
   static constexpr int kCBW = kSwz ? 128 : kRowBytes;
   static constexpr int kCB = kRowBytes / kCBW;
-  static constexpr int kCBBytes = kT * kCBW;
+  static constexpr int kCBBytes = kT * HP * kCBW;  // one column block of a stage's keys x heads
   static constexpr int kStageBytes = 2 * kCB * kCBBytes;  // K then V
   static constexpr bool kPermD = KV == KV_E4M3;     // fp8: permuted head dimension
   static constexpr int kMT = D / 16;                // O^T m-tiles of 16 d
@@ -46,9 +49,11 @@ struct DecCfg {
   // [4][kMT][32] float4; then the CTA's partial rows [8][D], maxima [8] and sums [8]
   static constexpr int kMergeBytes = kConsumerWarps * (2 * kRows + kMT * 32 * 4) * 4;
   static constexpr int kPartBytes = kRows * (D + 2) * 4;
-  // four consumer warps: three CTAs per SM, at most ~72 KB of shared memory each; eight:
-  // one CTA per SM
-  static constexpr int kBudget = W == 4 ? 72 * 1024 : 200 * 1024;
+  // four consumer warps: three CTAs per SM, at most ~72 KB of shared memory each; two
+  // kv-heads a CTA: two CTAs per SM with three 32 KB stages (the fp8 decode is bound by the
+  // SM's issue rate where three CTAs share an SM: measured 18.7 against 20.0 us for the
+  // sliding-window decode); eight consumer warps: one CTA per SM
+  static constexpr int kBudget = HP == 2 ? 100 * 1024 : W == 4 ? 72 * 1024 : 200 * 1024;
   static constexpr int kStagesFit = kBudget / kStageBytes;
   static constexpr int kStages = kStagesFit < 2 ? 2 : (kStagesFit > 6 ? 6 : kStagesFit);
   static constexpr int kPipeRaw = (kStages * kStageBytes > kMergeBytes + kPartBytes)
@@ -58,15 +63,26 @@ struct DecCfg {
   // fp8 per-token scales of a stage's keys, K then V, behind the barriers
   static constexpr int kScaleBytes = kPermD ? kStages * 2 * kT * 4 : 0;
   static constexpr int kSmemBytes = 1024 + kPipeBytes + 2 * kStages * 8 + kScaleBytes;
-  static constexpr int kMinBlocks = W != 4 ? 1 : (3 * (kSmemBytes + 1024) <= 228 * 1024) ? 3 : 2;
+  static constexpr int kMinBlocks = W != 4    ? 1
+                                   : HP == 2  ? 2
+                                   : (3 * (kSmemBytes + 1024) <= 228 * 1024) ? 3
+                                                                             : 2;
   static_assert(W == 4 || W == 8, "four or eight consumer warps");
   static_assert(D <= 128, "the key-major decode tile covers head_dim <= 128");
   static_assert(kRowBytes % kCBW == 0 && kCBW % 16 == 0, "rows are whole column blocks");
+  static_assert(HP == 1 || (HP == 2 && KV == KV_E4M3 && W == 4),
+                "two kv-heads a CTA: fp8 caches, four consumer warps");
 
-  // Byte offset of byte x of tile row r in a K or V stage.
-  static __device__ __forceinline__ uint32_t raw_byte(uint32_t r, uint32_t x) {
-    if constexpr (kSwz) return (x / 128) * kCBBytes + sw128(r, (x % 128) / 16) + (x & 15u);
-    else return r * kCBW + x;
+  // Line of head h's row of stage key r in a column block: a page box of HP heads lands
+  // head by head (16 lines each), so a line's swizzle phase is r mod 8 for every head.
+  static __device__ __forceinline__ uint32_t line(uint32_t r, uint32_t h) {
+    return HP == 1 ? r : ((r / 16) * HP + h) * 16 + (r % 16);
+  }
+  // Byte offset of byte x of head h's row of stage key r in a K or V stage.
+  static __device__ __forceinline__ uint32_t raw_byte(uint32_t r, uint32_t x, uint32_t h = 0) {
+    const uint32_t l = line(r, h);
+    if constexpr (kSwz) return (x / 128) * kCBBytes + sw128(l, (x % 128) / 16) + (x & 15u);
+    else return l * kCBW + x;
   }
   // Output column of O^T fragment row i (0..15) of m-tile m: the natural order, or (fp8)
   // the permuted order that makes each lane's V bytes one contiguous run.
@@ -77,19 +93,18 @@ struct DecCfg {
 };
 
 // QT: e4m3 terms of Q for fp8 caches (2 for a bf16 q, 3 for an f16 q); unused otherwise.
-// W: consumer warps of a CTA.
-template <int D, int KV, bool FEAT, int QT, int W>
-__global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>::kMinBlocks))
+// W: consumer warps of a CTA.  HP: kv-heads of a CTA (grid y = H_kv / HP).
+template <int D, int KV, bool FEAT, int QT, int W, int HP = 1>
+__global__ void __launch_bounds__(DecCfg<D, KV, W, HP>::kThreads,
+                                  (DecCfg<D, KV, W, HP>::kMinBlocks))
     ua_decode_kernel(const __grid_constant__ TileParams tp) {
-  using C = DecCfg<D, KV, W>;
+  using C = DecCfg<D, KV, W, HP>;
   constexpr int T = C::kT;
   constexpr int S = C::kStages;
   constexpr int NR = C::kRows;
+  constexpr int RH = C::kRH;
   constexpr bool kF16Mma = KvTraits<KV>::kF16Mma;
   const AttnParams& p = tp.p;
-  // Programmatic dependent launch (see the tile kernel).
-  grid_dependency_wait();
-  grid_launch_dependents();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
@@ -103,20 +118,44 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = blockIdx.y;
+  const int g = blockIdx.y * HP;  // first kv-head of the CTA
   const int z = blockIdx.z;
   const int G = p.group;
+  // fp8 per-token scales (aiter PR #3962 test matrix): key j's K and V rows carry their own
+  // scale, element (block, slot, g) of two separately strided arrays (one kv-head a CTA)
+  const bool tok = KV == KV_E4M3 && HP == 1 && p.k_scale_tok != nullptr;
 
-  // Slot x is sequence x (decode plans); its rows q_len x G of kv-head g, at most 8.
+  // Set-up that reads no input runs before the wait on the previous grid (programmatic
+  // dependent launch), so it overlaps that grid's tail: the barriers, and the cache
+  // tensor maps fetched into the descriptor cache.
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      // per-token scales: a second arrival once the stage's scales are in shared memory
+      mbar_init(&full[s], tok ? 2 : 1);
+      mbar_init(&empty[s], C::kConsumerWarps);
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == C::kConsumerWarps && lane == 0) {
+    tma_prefetch_desc(&tp.tmap_k);
+    tma_prefetch_desc(&tp.tmap_v);
+  }
+  __syncthreads();
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  // Slot x is sequence x (decode plans); its rows q_len x G of each kv-head, at most RH
+  // (8 / HP).  Column c of the q-block is row c mod RH of kv-head g + c / RH.
   const int b = static_cast<int>(blockIdx.x);
   const int q0 = __ldg(p.cu_seqlens_q + b);
   const int q_len = __ldg(p.cu_seqlens_q + b + 1) - q0;
   const int kv_len = __ldg(p.seq_lens_k + b);
   const int rows_b = q_len * G;
-  if (rows_b > NR && threadIdx.x == 0 && z == 0 && g == 0)
-    atomicOr(p.status, DEV_BAD_SHAPE);  // q_len above max_seqlen_q: rows past 8 unwritten
+  if (rows_b > RH && threadIdx.x == 0 && z == 0 && g == 0)
+    atomicOr(p.status, DEV_BAD_SHAPE);  // q_len above max_seqlen_q: rows past RH unwritten
   if (rows_b <= 0) return;              // idle slot: uniform for the slot's cluster
-  const int nr = min(rows_b, NR);
+  const int nr = min(rows_b, RH);
   const int ctx = kv_len - q_len;
   const int pos_first = ctx;
   const int pos_last = ctx + (nr - 1) / G;
@@ -129,20 +168,6 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
   const int ke = min(ks + part, hi);
   const int ntiles = (ke - ks + T - 1) / T;
   const bool cmerge = p.cluster_merge != 0;
-  // fp8 per-token scales (aiter PR #3962 test matrix): key j's K and V rows carry their own
-  // scale, element (block, slot, g) of two separately strided arrays
-  const bool tok = KV == KV_E4M3 && p.k_scale_tok != nullptr;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      // per-token scales: a second arrival once the stage's scales are in shared memory
-      mbar_init(&full[s], tok ? 2 : 1);
-      mbar_init(&empty[s], C::kConsumerWarps);
-    }
-    s_abort = 0;
-    mbar_fence_init();
-  }
-  __syncthreads();
 
   if (warp == C::kConsumerWarps) {
     // ======================================================== producer warp
@@ -153,6 +178,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
     const uint64_t policy = l2_policy_evict_first();
     const int bs = p.block_size;
     const int oob = p.num_blocks * bs;
+    // this lane's cache row of tile t
     auto page_row = [&](int t) -> int {
       const int key = ks + t * T + 16 * lane;
       if (lane >= T / 16 || key >= ke) return oob;
@@ -164,6 +190,27 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
       }
       return blk * bs + key % bs;
     };
+    // one stage's page boxes, K and V, on stage s's full barrier
+    auto issue = [&](int s, int row) {
+      uint8_t* kdst = pipe + s * C::kStageBytes;
+      uint8_t* vdst = kdst + C::kCB * C::kCBBytes;
+      if (lane < T / 16) {
+#pragma unroll
+        for (int cb = 0; cb < C::kCB; ++cb) {
+          const int x = cb * (C::kCBW / C::kEsz);
+          uint8_t* const kd = kdst + cb * C::kCBBytes + lane * 16 * HP * C::kCBW;
+          uint8_t* const vd = vdst + cb * C::kCBBytes + lane * 16 * HP * C::kCBW;
+          if constexpr (HP == 1) {  // view [row][head][d]: box {cols, 1 head, 16 rows}
+            tma_load_3d(kd, &tp.tmap_k, x, g, row, &full[s], policy);
+            tma_load_3d(vd, &tp.tmap_v, x, g, row, &full[s], policy);
+          } else {  // view [head][row][d]: box {cols, 16 rows, HP heads}, head by head
+            tma_load_3d(kd, &tp.tmap_k, x, row, g, &full[s], policy);
+            tma_load_3d(vd, &tp.tmap_v, x, row, g, &full[s], policy);
+          }
+        }
+      }
+    };
+    int issued = 0;
     // Per-token scales of this lane's kKPL keys kKPL lane .. of tile t (one page; 0 past
     // the walk): the page's block id is loaded two tiles ahead, the scales one tile ahead.
     constexpr int KPL = C::kKPL;
@@ -181,10 +228,10 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
         const int key = ks + t * T + KPL * lane + e;
         if (blk < 0 || key >= ke) continue;
         const long long slot = key % bs;
-        kv[e][0] = __ldg(p.k_scale_tok + blk * p.k_scale_stride[0] + slot * p.k_scale_stride[1] +
-                         g * p.k_scale_stride[2]);
-        kv[e][1] = __ldg(p.v_scale_tok + blk * p.v_scale_stride[0] + slot * p.v_scale_stride[1] +
-                         g * p.v_scale_stride[2]);
+        kv[e][0] = __ldg(p.k_scale_tok + blk * p.k_scale_stride[0] +
+                         slot * p.k_scale_stride[1] + g * p.k_scale_stride[2]);
+        kv[e][1] = __ldg(p.v_scale_tok + blk * p.v_scale_stride[0] +
+                         slot * p.v_scale_stride[1] + g * p.v_scale_stride[2]);
       }
     };
     float sc_next[KPL][2];
@@ -195,7 +242,6 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
       if (ntiles > 0) load_scales(0, scale_blk(0), sc_next);
       blk_next = scale_blk(1);
     }
-    int issued = 0;
     int row_next = ntiles > 0 ? page_row(0) : oob;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % S;
@@ -213,20 +259,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
       }
       if (t >= S && !mbar_wait_bounded(&empty[s], ((t / S) & 1) ^ 1, p.status, DEV_TIMEOUT))
         break;
-      uint8_t* kdst = pipe + s * C::kStageBytes;
-      uint8_t* vdst = kdst + C::kCB * C::kCBBytes;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
       __syncwarp();
-      if (lane < T / 16) {
-#pragma unroll
-        for (int cb = 0; cb < C::kCB; ++cb) {
-          const int x = cb * (C::kCBW / C::kEsz);
-          tma_load_3d(kdst + cb * C::kCBBytes + lane * 16 * C::kCBW, &tp.tmap_k, x, g, row,
-                      &full[s], policy);
-          tma_load_3d(vdst + cb * C::kCBBytes + lane * 16 * C::kCBW, &tp.tmap_v, x, g, row,
-                      &full[s], policy);
-        }
-      }
+      issue(s, row);
       if (tok) {  // after the copies are on their way; released to the consumers by lane 0
 #pragma unroll
         for (int e = 0; e < KPL; ++e) {
@@ -243,7 +278,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
       mbar_wait_bounded(&full[t % S], (t / S) & 1, p.status, DEV_TIMEOUT);
     if (cmerge) {  // the consumers' two cluster barriers
       cluster_sync();
-      cluster_sync();
+      cluster_sync_relaxed();
     }
     return;
   }
@@ -260,16 +295,17 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
   }
   const float scale = p.scale * k_scale;
 
-  // The accumulator rows of this lane: 2cq and 2cq + 1 (N columns of the S^T / O^T tiles).
+  // The accumulator rows of this lane: 2cq and 2cq + 1 (N columns of the S^T / O^T tiles),
+  // rows r of kv-head g + c / RH.
   bool rv[2];
   int rh[2], ri[2], rpos[2], rlo[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    const int r = 2 * cq + e;
+    const int c = 2 * cq + e, r = c % RH;
     rv[e] = r < nr && q0 + r / G < p.total_q;  // never index past the q / out tensors
     const int i = rv[e] ? r / G : 0;
     ri[e] = i;
-    rh[e] = g * G + (rv[e] ? r % G : 0);
+    rh[e] = (g + c / RH) * G + (rv[e] ? r % G : 0);
     rpos[e] = ctx + i;
     rlo[e] = p.window_left >= 0 ? max(0, rpos[e] - p.window_left) : 0;
   }
@@ -296,10 +332,11 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
   uint32_t q8[kQT][C::kPermD ? D / 32 : 1][2];
   float row_scale[2] = {1.f, 1.f};  // 2^-c of rows 2cq and 2cq + 1 (fp8)
   {
-    const bool qv = gq < nr && q0 + gq / G < p.total_q;
+    const int rq = gq % RH;  // column gq: row rq of kv-head g + gq / RH
+    const bool qv = rq < nr && q0 + rq / G < p.total_q;
     const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
-                           (static_cast<size_t>(q0 + (qv ? gq / G : 0)) * p.hq + g * G +
-                            (qv ? gq % G : 0)) *
+                           (static_cast<size_t>(q0 + (qv ? rq / G : 0)) * p.hq +
+                            (g + gq / RH) * G + (qv ? rq % G : 0)) *
                                D;
     if constexpr (!C::kPermD) {
 #pragma unroll
@@ -429,19 +466,50 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
         for (int term = 0; term < kQT; ++term)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sx[term][e] = 0.f;
+        if constexpr (HP == 1) {
 #pragma unroll
-        for (int u = 0; u < D / 64; ++u) {
-          const uint4 k0 = *reinterpret_cast<const uint4*>(
-              kst + C::raw_byte(16 * ch + gq, cq * (D / 4) + 16 * u));
-          const uint4 k8 = *reinterpret_cast<const uint4*>(
-              kst + C::raw_byte(16 * ch + gq + 8, cq * (D / 4) + 16 * u));
+          for (int u = 0; u < D / 64; ++u) {
+            const uint4 k0 = *reinterpret_cast<const uint4*>(
+                kst + C::raw_byte(16 * ch + gq, cq * (D / 4) + 16 * u));
+            const uint4 k8 = *reinterpret_cast<const uint4*>(
+                kst + C::raw_byte(16 * ch + gq + 8, cq * (D / 4) + 16 * u));
 #pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            const uint32_t a[4] = {tt ? k0.z : k0.x, tt ? k8.z : k8.x, tt ? k0.w : k0.y,
-                                   tt ? k8.w : k8.y};
+            for (int tt = 0; tt < 2; ++tt) {
+              const uint32_t a[4] = {tt ? k0.z : k0.x, tt ? k8.z : k8.x, tt ? k0.w : k0.y,
+                                     tt ? k8.w : k8.y};
 #pragma unroll
-            for (int term = 0; term < kQT; ++term)
-              mma_16832_e4m3(sx[term], a, q8[term][2 * u + tt][0], q8[term][2 * u + tt][1]);
+              for (int term = 0; term < kQT; ++term)
+                mma_16832_e4m3(sx[term], a, q8[term][2 * u + tt][0], q8[term][2 * u + tt][1]);
+            }
+          }
+        } else {
+          // Two kv-heads: k-step j of chunk u pairs word j of head g's rows (k 0..15 of the
+          // MMA) with word j of head g + 1's rows (k 16..31).  The B operand is block
+          // diagonal: a lane's Q word (its column's head) goes to b0 for a column of head g
+          // and to b1 for head g + 1, the other half zero, so each column sums over its own
+          // head's keys only.
+          const uint32_t bm0 = gq < RH ? 0xffffffffu : 0u, bm1 = ~bm0;
+#pragma unroll
+          for (int u = 0; u < D / 64; ++u) {
+            const uint4 x0 = *reinterpret_cast<const uint4*>(
+                kst + C::raw_byte(16 * ch + gq, cq * (D / 4) + 16 * u, 0));
+            const uint4 x8 = *reinterpret_cast<const uint4*>(
+                kst + C::raw_byte(16 * ch + gq + 8, cq * (D / 4) + 16 * u, 0));
+            const uint4 y0 = *reinterpret_cast<const uint4*>(
+                kst + C::raw_byte(16 * ch + gq, cq * (D / 4) + 16 * u, 1));
+            const uint4 y8 = *reinterpret_cast<const uint4*>(
+                kst + C::raw_byte(16 * ch + gq + 8, cq * (D / 4) + 16 * u, 1));
+            const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w8[4] = {x8.x, x8.y, x8.z, x8.w};
+            const uint32_t v0[4] = {y0.x, y0.y, y0.z, y0.w}, v8[4] = {y8.x, y8.y, y8.z, y8.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t a[4] = {w0[j], w8[j], v0[j], v8[j]};
+#pragma unroll
+              for (int term = 0; term < kQT; ++term) {
+                const uint32_t qw = q8[term][2 * u + j / 2][j & 1];
+                mma_16832_e4m3(sx[term], a, qw & bm0, qw & bm1);
+              }
+            }
           }
         }
 #pragma unroll
@@ -565,48 +633,55 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
         // Lane (gq, cq) reads bytes [gq D/8, (gq + 1) D/8) of V rows 2cq, 2cq+1, 2cq+8,
         // 2cq+9; bytes 2m and 2m + 1 of that run are fragment rows gq and gq + 8 of
         // m-tile m (output columns gq D/8 + 2m and + 1).  A byte permute pairs the two
-        // keys of each operand half.
+        // keys of each operand half.  Two kv-heads: one pass per head, with P^T's columns
+        // of the other head zeroed, so both heads accumulate into their own columns of O^T.
         constexpr int kW = D / 32;  // 32-bit words of a row per lane
-        uint32_t vw[4][kW];
 #pragma unroll
-        for (int r4 = 0; r4 < 4; ++r4) {
-          const uint32_t trow = 16 * ch + 2 * cq + (r4 & 1) + 8 * (r4 >> 1);
-          if constexpr (kW % 4 == 0) {
+        for (int hh = 0; hh < HP; ++hh) {
+          const uint32_t bm = HP == 1 || (gq / RH) == hh ? 0xffffffffu : 0u;
+          const uint32_t pv0 = pb[0] & bm, pv1 = pb[1] & bm;
+          uint32_t vw[4][kW];
 #pragma unroll
-            for (int x = 0; x < kW; x += 4) {
-              const uint4 v4 =
-                  *reinterpret_cast<const uint4*>(vst + C::raw_byte(trow, gq * (D / 8) + 4 * x));
-              vw[r4][x] = v4.x;
-              vw[r4][x + 1] = v4.y;
-              vw[r4][x + 2] = v4.z;
-              vw[r4][x + 3] = v4.w;
+          for (int r4 = 0; r4 < 4; ++r4) {
+            const uint32_t trow = 16 * ch + 2 * cq + (r4 & 1) + 8 * (r4 >> 1);
+            if constexpr (kW % 4 == 0) {
+#pragma unroll
+              for (int x = 0; x < kW; x += 4) {
+                const uint4 v4 = *reinterpret_cast<const uint4*>(
+                    vst + C::raw_byte(trow, gq * (D / 8) + 4 * x, hh));
+                vw[r4][x] = v4.x;
+                vw[r4][x + 1] = v4.y;
+                vw[r4][x + 2] = v4.z;
+                vw[r4][x + 3] = v4.w;
+              }
+            } else {
+              const uint2 v2 =
+                  *reinterpret_cast<const uint2*>(vst + C::raw_byte(trow, gq * (D / 8), hh));
+              vw[r4][0] = v2.x;
+              vw[r4][1] = v2.y;
             }
-          } else {
-            const uint2 v2 = *reinterpret_cast<const uint2*>(vst + C::raw_byte(trow, gq * (D / 8)));
-            vw[r4][0] = v2.x;
-            vw[r4][1] = v2.y;
           }
-        }
 #pragma unroll
-        for (int x = 0; x < kW; ++x) {
-          // bytes 4x, 4x + 1 (m-tile 2x) then 4x + 2, 4x + 3 (m-tile 2x + 1) of the rows
-          const uint32_t lo0 = __byte_perm(vw[0][x], vw[1][x], 0x5140);
-          const uint32_t hi0 = __byte_perm(vw[0][x], vw[1][x], 0x7362);
-          const uint32_t lo8 = __byte_perm(vw[2][x], vw[3][x], 0x5140);
-          const uint32_t hi8 = __byte_perm(vw[2][x], vw[3][x], 0x7362);
+          for (int x = 0; x < kW; ++x) {
+            // bytes 4x, 4x + 1 (m-tile 2x) then 4x + 2, 4x + 3 (m-tile 2x + 1) of the rows
+            const uint32_t lo0 = __byte_perm(vw[0][x], vw[1][x], 0x5140);
+            const uint32_t hi0 = __byte_perm(vw[0][x], vw[1][x], 0x7362);
+            const uint32_t lo8 = __byte_perm(vw[2][x], vw[3][x], 0x5140);
+            const uint32_t hi8 = __byte_perm(vw[2][x], vw[3][x], 0x7362);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t w0 = h ? hi0 : lo0, w8 = h ? hi8 : lo8;
-            uint32_t a[4];
-            e4m3x4_to_f16x4(w0, a[0], a[1]);
-            e4m3x4_to_f16x4(w8, a[2], a[3]);
-            if (tail) {
-              a[0] &= m01;
-              a[1] &= m01;
-              a[2] &= m89;
-              a[3] &= m89;
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t w0 = h ? hi0 : lo0, w8 = h ? hi8 : lo8;
+              uint32_t a[4];
+              e4m3x4_to_f16x4(w0, a[0], a[1]);
+              e4m3x4_to_f16x4(w8, a[2], a[3]);
+              if (tail) {
+                a[0] &= m01;
+                a[1] &= m01;
+                a[2] &= m89;
+                a[3] &= m89;
+              }
+              mma_16816<true>(ot[2 * x + h], a, pv0, pv1);
             }
-            mma_16816<true>(ot[2 * x + h], a, pb[0], pb[1]);
           }
         }
       } else {
@@ -721,17 +796,24 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
 
   const size_t n_part = static_cast<size_t>(p.n_part);
   const size_t esz = p.out_dtype == UA_DT_F32 ? 4 : 2;
-  // output row of q-block row r (valid for r < nr with its token inside the batch)
-  auto out_row = [&](int r) -> size_t {
-    return static_cast<size_t>(q0 + r / G) * p.hq + g * G + r % G;
+  // q-block column c holds row c mod RH of kv-head g + c / RH: a row when that is below
+  // nr and its token lies inside the batch
+  auto col_valid = [&](int c) -> bool {
+    const int r = c % RH;
+    return r < nr && q0 + r / G < p.total_q;
   };
+  auto out_row = [&](int c) -> size_t {
+    const int r = c % RH;
+    return static_cast<size_t>(q0 + r / G) * p.hq + (g + c / RH) * G + r % G;
+  };
+  const int ncols = HP == 1 ? nr : NR;  // columns up to the last that may hold a row
   if (n_part == 1 || !cmerge) {
     if (!ok) return;
     // one partition: normalised rows; several: the partition's max / sum / output rows
     // in the global scratch for the merge kernel
-    for (int idx = threadIdx.x; idx < nr * D; idx += 32 * C::kConsumerWarps) {
+    for (int idx = threadIdx.x; idx < ncols * D; idx += 32 * C::kConsumerWarps) {
       const int r = idx / D, c = idx % D;
-      if (q0 + r / G >= p.total_q) continue;
+      if (!col_valid(r)) continue;
       const size_t row = out_row(r);
       const float v = partial[r * D + c];
       if (n_part == 1) {
@@ -753,79 +835,34 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W>::kThreads, (DecCfg<D, KV, W>:
     return;
   }
 
-  // Cluster merge: the cluster is the n_part partitions (grid z) of cluster_y kv-heads of
-  // this slot; partition zz of this kv-head is the cluster's CTA cluster_ctaid.y +
-  // cluster_y * zz.  Row r is merged by partition r mod n_part, one warp a row (the LSE
-  // merge of the split path):
-  //   M = max_{l_z > 0} m_z,  L = sum l_z 2^(m_z - M),  out = sum acc_z 2^(m_z - M) / L.
+  // Cluster merge: the cluster is the n_part partitions (grid z) of cluster_y CTAs (kv-heads,
+  // or pairs of them) of this slot; partition zz of this CTA's heads is the cluster's CTA
+  // cluster_ctaid.y + cluster_y * zz.  Column r is merged by partition r mod n_part, one
+  // warp a row.
   cluster_sync();
   {
-    constexpr int kPer = D / 32;
     const int np = p.n_part;
     const uint32_t cy = cluster_nctaid_y(), yc = cluster_ctaid_y();
     const uint32_t part_s = smem_addr(partial);
     for (int k = warp;; k += C::kConsumerWarps) {
       const int r = z + np * k;
-      if (r >= nr) break;
-      if (q0 + r / G >= p.total_q) break;
-      const size_t orow = out_row(r);
-      float mz = -INFINITY, lz = 0.f;
-      if (lane < np) {
-        const uint32_t rank = yc + cy * lane;
-        mz = ld_cluster_f32(cluster_map(part_s + (NR * D + r) * 4, rank));
-        lz = ld_cluster_f32(cluster_map(part_s + (NR * D + NR + r) * 4, rank));
-      }
-      float M = lz > 0.f ? mz : -INFINITY;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float wz = (lz > 0.f && M != -INFINITY) ? fast_exp2(mz - M) : 0.f;
-      float L = lz * wz;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      float acc[kPer];
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-      for (int zz = 0; zz < np; ++zz) {
-        const float wt = __shfl_sync(0xffffffffu, wz, zz);
-        if (wt == 0.f) continue;  // uniform: an empty partition
-        const uint32_t a = cluster_map(part_s + (r * D + lane * kPer) * 4, yc + cy * zz);
-        if constexpr (kPer >= 4) {
-#pragma unroll
-          for (int e = 0; e < kPer; e += 4) {
-            const float4 v = ld_cluster_f32x4(a + e * 4);
-            acc[e] += v.x * wt;
-            acc[e + 1] += v.y * wt;
-            acc[e + 2] += v.z * wt;
-            acc[e + 3] += v.w * wt;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) acc[e] += ld_cluster_f32(a + e * 4) * wt;
-        }
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      uint8_t* dst = static_cast<uint8_t*>(p.out) + orow * D * esz;
-#pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        const int col = lane * kPer + e;
-        const float x0 = acc[e] * inv, x1 = acc[e + 1] * inv;
-        if (p.out_dtype == UA_DT_F32) {
-          *reinterpret_cast<float2*>(reinterpret_cast<float*>(dst) + col) = make_float2(x0, x1);
-        } else {
-          const uint32_t v = p.out_dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
-          *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(dst) + col) = v;
-        }
-      }
+      if (r >= ncols) break;
+      if (!col_valid(r)) continue;
+      cluster_merge_row<D>(part_s + (NR * D + r) * 4, part_s + (NR * D + NR + r) * 4,
+                           part_s + r * D * 4, np, yc, cy, lane,
+                           static_cast<uint8_t*>(p.out) + out_row(r) * D * esz, p.out_dtype);
     }
   }
-  cluster_sync();  // no CTA leaves while the cluster still reads its shared memory
+  // no CTA leaves while the cluster still reads its shared memory (those reads have
+  // returned: a relaxed arrival, which need not wait for the output stores)
+  cluster_sync_relaxed();
 }
 
-template <int D, int KV, bool FEAT, int QT, int W>
+template <int D, int KV, bool FEAT, int QT, int W, int HP = 1>
 cudaError_t launch_decode_t(const TileParams& tp, dim3 grid, int cluster_y, int cluster_z,
                             cudaStream_t stream) {
-  using C = DecCfg<D, KV, W>;
-  auto kern = ua_decode_kernel<D, KV, FEAT, QT, W>;
+  using C = DecCfg<D, KV, W, HP>;
+  auto kern = ua_decode_kernel<D, KV, FEAT, QT, W, HP>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -858,13 +895,25 @@ cudaError_t launch_decode_width(const TileParams& tp, dim3 grid, int kv, bool fe
   return cudaErrorInvalidValue;
 }
 
+// Two kv-heads a CTA (fp8 caches, four consumer warps; tensor maps over the head-outer
+// view with boxes of two heads).
+template <int D>
+cudaError_t launch_decode_pair(const TileParams& tp, dim3 grid, bool feat, int cluster_y,
+                               int cluster_z, cudaStream_t s) {
+  if (tp.p.q_dtype == UA_DT_BF16)
+    return feat ? launch_decode_t<D, KV_E4M3, true, 2, 4, 2>(tp, grid, cluster_y, cluster_z, s)
+                : launch_decode_t<D, KV_E4M3, false, 2, 4, 2>(tp, grid, cluster_y, cluster_z, s);
+  return feat ? launch_decode_t<D, KV_E4M3, true, 3, 4, 2>(tp, grid, cluster_y, cluster_z, s)
+              : launch_decode_t<D, KV_E4M3, false, 3, 4, 2>(tp, grid, cluster_y, cluster_z, s);
+}
+
 // Clusters of cluster_y x cluster_z CTAs of the decode kernel that can be resident at
 // once (the hardware places a cluster's CTAs within one GPU processing cluster, so fewer
 // CTAs than the SMs' slots may run together); -1 when the query fails.
-template <int D, int KV, int W>
+template <int D, int KV, int W, int HP = 1>
 int decode_cluster_capacity_t(int cluster_y, int cluster_z) {
-  using C = DecCfg<D, KV, W>;
-  auto kern = ua_decode_kernel<D, KV, false, KV == KV_E4M3 ? 2 : 1, W>;
+  using C = DecCfg<D, KV, W, HP>;
+  auto kern = ua_decode_kernel<D, KV, false, KV == KV_E4M3 ? 2 : 1, W, HP>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
           cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)

@@ -113,6 +113,12 @@ __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Fetch a TMA descriptor (a __grid_constant__ kernel parameter) into the descriptor cache
+// ahead of its first use.
+__device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(desc)) : "memory");
+}
+
 // Allow the next grid on the stream to be scheduled before this one completes.
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -160,6 +166,12 @@ inline cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size
 // writes before it are visible to the cluster's CTAs after it.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The same barrier with a relaxed arrival: for the last barrier of a cluster, whose only
+// job is that no CTA exits while another still reads its shared memory (reads whose values
+// are already in registers); earlier writes, global stores included, need not drain.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t cluster_ctaid_y() {
   uint32_t r;

@@ -103,11 +103,20 @@ cudaError_t launch_decode_w8_d64(const TileParams& tp, dim3 grid, int kv, bool f
                                  int cluster_y, int cluster_z, cudaStream_t s);
 cudaError_t launch_decode_w8_d128(const TileParams& tp, dim3 grid, int kv, bool feat,
                                   int cluster_y, int cluster_z, cudaStream_t s);
+// the same tile with two kv-heads per CTA (fp8 caches, at most 4 rows per kv-head; tensor
+// maps over the view [H_kv][rows][D] with boxes of two heads)
+cudaError_t launch_decode_pair_d64(const TileParams& tp, dim3 grid, bool feat, int cluster_y,
+                                   int cluster_z, cudaStream_t s);
+cudaError_t launch_decode_pair_d128(const TileParams& tp, dim3 grid, bool feat, int cluster_y,
+                                    int cluster_z, cudaStream_t s);
+int decode_cluster_capacity_pair(int head_dim, int cluster_y, int cluster_z);
+int decode_pair_ctas_per_sm(int head_dim);
 // resident CTAs per SM of the four-warp decode tile
 int decode_ctas_per_sm(int head_dim, int kv);
 // co-resident clusters of cluster_y x cluster_z decode CTAs (four or, wide, eight consumer
-// warps) on the current device (-1: unknown); cached per device
-int decode_cluster_capacity(int head_dim, int kv, bool wide, int cluster_y, int cluster_z);
+// warps; pair: two kv-heads a CTA) on the current device (-1: unknown); cached per device
+int decode_cluster_capacity(int head_dim, int kv, bool wide, bool pair, int cluster_y,
+                            int cluster_z);
 int decode_cluster_capacity_w8(int head_dim, int kv, int cluster_y, int cluster_z);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_prefill_d64(const PrefillParams& pp, dim3 grid, int kv, bool feat, int nq,
@@ -119,7 +128,7 @@ cudaError_t launch_prefill_d256(const PrefillParams& pp, dim3 grid, int kv, bool
 
 // Plan kernel codes.
 enum : int { KERNEL_TILE16 = 1, KERNEL_DEC8 = 2, KERNEL_TILE64 = 4, KERNEL_TC128 = 8, KERNEL_TC256 = 16,
-             KERNEL_DEC8W = 32 };
+             KERNEL_DEC8W = 32, KERNEL_DEC8P = 64 };
 
 // Resident CTAs per SM of the tile kernel variant for (head_dim, kv dtype, wm).
 int tile_ctas_per_sm(int head_dim, int kv, int wm);

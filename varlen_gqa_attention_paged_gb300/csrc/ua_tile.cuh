@@ -186,6 +186,88 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// LSE merge of one output row over the np (<= 16) split partitions of a thread-block
+// cluster, by one warp (the merge of the split path):
+//   M = max_{l_z > 0} m_z,  L = sum l_z 2^(m_z - M),  out = sum acc_z 2^(m_z - M) / L.
+// Partition zz is the cluster's CTA rank0 + rank_step * zz; in its shared memory the row's
+// max and sum sit at byte offsets m_off and l_off and its partial row (D floats) at
+// row_off.  Every partition's max, sum and slice of the row are loaded before any is used
+// (at most 64 floats a lane in flight), so the round trips through distributed shared
+// memory overlap.  An empty partition weighs 0 (its partial row is 0).  Writes the
+// normalised row to dst in out_dtype.
+template <int D>
+__device__ __forceinline__ void cluster_merge_row(uint32_t m_off, uint32_t l_off,
+                                                  uint32_t row_off, int np, uint32_t rank0,
+                                                  uint32_t rank_step, int lane, uint8_t* dst,
+                                                  int out_dtype) {
+  constexpr int kPer = D / 32;                     // columns a lane merges
+  constexpr int kBatch = kPer > 4 ? 64 / kPer : 16;  // partitions loaded at once
+  float mz = -INFINITY, lz = 0.f;
+  if (lane < np) {
+    const uint32_t rank = rank0 + rank_step * lane;
+    mz = ld_cluster_f32(cluster_map(m_off, rank));
+    lz = ld_cluster_f32(cluster_map(l_off, rank));
+  }
+  float v[kBatch][kPer];
+  auto load = [&](int z0) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) v[i][e] = 0.f;
+      if (z0 + i < np) {
+        const uint32_t a = cluster_map(row_off + lane * kPer * 4, rank0 + rank_step * (z0 + i));
+        if constexpr (kPer >= 4) {
+#pragma unroll
+          for (int e = 0; e < kPer; e += 4) {
+            const float4 x = ld_cluster_f32x4(a + e * 4);
+            v[i][e] = x.x;
+            v[i][e + 1] = x.y;
+            v[i][e + 2] = x.z;
+            v[i][e + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) v[i][e] = ld_cluster_f32(a + e * 4);
+        }
+      }
+    }
+  };
+  load(0);
+  float M = lz > 0.f ? mz : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float wz = (lz > 0.f && M != -INFINITY) ? fast_exp2(mz - M) : 0.f;
+  float L = lz * wz;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int z0 = 0; z0 < np; z0 += kBatch) {
+    if (z0 > 0) load(z0);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (z0 + i < np) {  // uniform
+        const float wt = __shfl_sync(0xffffffffu, wz, z0 + i);
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] += v[i][e] * wt;
+      }
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2) {
+    const int col = lane * kPer + e;
+    const float x0 = acc[e] * inv, x1 = acc[e + 1] * inv;
+    if (out_dtype == UA_DT_F32) {
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(dst) + col) = make_float2(x0, x1);
+    } else {
+      const uint32_t w = out_dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(dst) + col) = w;
+    }
+  }
+}
+
 template <int D, int KV, int WM, bool FEAT, bool TMA>
 __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
     ua_attn_tile_kernel(const __grid_constant__ TileParams tp) {
@@ -195,12 +277,6 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
   constexpr bool kF16Mma = KvTraits<KV>::kF16Mma;
   constexpr int BM = 16 * WM;
   const AttnParams& p = tp.p;
-  // Programmatic dependent launch: this grid may be scheduled while the previous kernel
-  // on the stream finishes; it reads nothing before that kernel has completed, and lets
-  // the next kernel (the merge) be scheduled early in turn.
-  grid_dependency_wait();
-  grid_launch_dependents();
-
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,6 +290,28 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
   const int g = blockIdx.y;
   const int z = blockIdx.z;
   const int G = p.group;
+
+  // Programmatic dependent launch: this grid may be scheduled while the previous kernel
+  // on the stream finishes.  Set-up that reads no input (the barriers, the tensor maps
+  // fetched into the descriptor cache) runs before the wait on that kernel; everything
+  // else after it.  The next kernel (the merge) is let in early in turn.
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::kConsumerWarps);
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if constexpr (TMA) {
+    if (warp == C::kConsumerWarps && lane == 0) {
+      tma_prefetch_desc(&tp.tmap_k);
+      tma_prefetch_desc(&tp.tmap_v);
+    }
+  }
+  __syncthreads();
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // ---- which rows and keys this CTA owns.  Slot x is sequence x when every sequence
   // fits one q-block (decode batches: no search); otherwise a binary search over
@@ -242,16 +340,6 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
   const int ks = min(lo + z * part, hi);
   const int ke = min(ks + part, hi);
   const int ntiles = (ke - ks + T - 1) / T;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::kConsumerWarps);
-    }
-    s_abort = 0;
-    mbar_fence_init();
-  }
-  __syncthreads();
 
   if (warp == C::kConsumerWarps) {
     // ======================================================== producer warp
@@ -347,7 +435,7 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
       mbar_wait_bounded(&full[t % S], (t / S) & 1, p.status, DEV_TIMEOUT);
     if (WM == 1 && p.cluster_merge) {  // the consumers' two cluster barriers
       cluster_sync();
-      cluster_sync();
+      cluster_sync_relaxed();
     }
     return;
   }
@@ -775,11 +863,9 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
   // Cluster merge: the cluster is the n_part partitions (grid z) of cluster_y kv-heads of
   // this q-block slot; partition zz of this kv-head is the cluster's CTA
   // cluster_ctaid.y + cluster_y * zz.  Row r of the q-block is merged by partition
-  // r mod n_part, one warp a row (the LSE merge of the split path):
-  //   M = max_{l_z > 0} m_z,  L = sum l_z 2^(m_z - M),  out = sum acc_z 2^(m_z - M) / L.
+  // r mod n_part, one warp a row.
   cluster_sync();
   {
-    constexpr int kPer = D / 32;
     const int np = p.n_part;
     const uint32_t cy = cluster_nctaid_y(), yc = cluster_ctaid_y();
     const uint32_t part_s = smem_addr(partial);
@@ -790,56 +876,14 @@ __global__ void __launch_bounds__(160, (TileCfg<D, KV, WM>::kMinBlocks))
       const int tok = q0 + (r0 + r) / G;
       if (tok >= p.total_q) break;
       const size_t orow = static_cast<size_t>(tok) * p.hq + g * G + (r0 + r) % G;
-      float mz = -INFINITY, lz = 0.f;
-      if (lane < np) {
-        const uint32_t rank = yc + cy * lane;
-        mz = ld_cluster_f32(cluster_map(part_s + (16 * D + r) * 4, rank));
-        lz = ld_cluster_f32(cluster_map(part_s + (16 * D + 16 + r) * 4, rank));
-      }
-      float M = lz > 0.f ? mz : -INFINITY;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float wz = (lz > 0.f && M != -INFINITY) ? fast_exp2(mz - M) : 0.f;
-      float L = lz * wz;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      float acc[kPer];
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-      for (int zz = 0; zz < np; ++zz) {
-        const float wt = __shfl_sync(0xffffffffu, wz, zz);
-        if (wt == 0.f) continue;  // uniform: an empty partition
-        const uint32_t a = cluster_map(part_s + (r * D + lane * kPer) * 4, yc + cy * zz);
-#pragma unroll
-        for (int e = 0; e < kPer; e += 4) {
-          if constexpr (kPer >= 4) {
-            const float4 v = ld_cluster_f32x4(a + e * 4);
-            acc[e] += v.x * wt;
-            acc[e + 1] += v.y * wt;
-            acc[e + 2] += v.z * wt;
-            acc[e + 3] += v.w * wt;
-          } else {
-#pragma unroll
-            for (int f = 0; f < kPer; ++f) acc[f] += ld_cluster_f32(a + f * 4) * wt;
-          }
-        }
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      uint8_t* dst = static_cast<uint8_t*>(p.out) + orow * D * esz;
-#pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        const int col = lane * kPer + e;
-        const float x0 = acc[e] * inv, x1 = acc[e + 1] * inv;
-        if (p.out_dtype == UA_DT_F32) {
-          *reinterpret_cast<float2*>(reinterpret_cast<float*>(dst) + col) = make_float2(x0, x1);
-        } else {
-          const uint32_t v = p.out_dtype == UA_DT_BF16 ? pack_bf16(x0, x1) : pack_f16(x0, x1);
-          *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(dst) + col) = v;
-        }
-      }
+      cluster_merge_row<D>(part_s + (16 * D + r) * 4, part_s + (16 * D + 16 + r) * 4,
+                           part_s + r * D * 4, np, yc, cy, lane,
+                           static_cast<uint8_t*>(p.out) + orow * D * esz, p.out_dtype);
     }
   }
-  cluster_sync();  // no CTA leaves while the cluster still reads its shared memory
+  // no CTA leaves while the cluster still reads its shared memory (those reads have
+  // returned: a relaxed arrival, which need not wait for the output stores)
+  cluster_sync_relaxed();
 }
 
 template <int D, int KV, int WM, bool FEAT, bool TMA>
