@@ -351,10 +351,12 @@ def e2e_pipelined(inp, call, dev, stream, reps, steps):
 
     A step's inputs (q, cu_seqlens_q, seq_lens_k and the block table of the step's cache
     replica) sit in one pinned host buffer and travel in one host-to-device copy; its
-    output comes back in one device-to-host copy into pinned memory.  Copies run on a copy
-    stream and the attention calls on the compute stream, each with two device buffers
-    used in turn, so step i's copies overlap step i-1's kernel (events order each buffer's
-    reuse).  Time: host wall clock from a synchronised start to a synchronised end.
+    output comes back in one device-to-host copy into pinned memory.  The input copies,
+    the attention calls and the output copies run on three streams, with two device
+    buffers used in turn, so step i's input copy and step i-1's output copy overlap step
+    i-1's and step i's kernels (one copy stream would queue step i's input behind step
+    i-1's output, which waits for step i-1's kernel); events order each buffer's reuse.
+    Time: host wall clock from a synchronised start to a synchronised end.
     Returns (milliseconds, host-to-device bytes a step, device-to-host bytes a step)."""
     import varlen_gqa_attention_paged_gb300 as ua
     rt = Cudart()
@@ -372,8 +374,9 @@ def e2e_pipelined(inp, call, dev, stream, reps, steps):
         for t, o, n in zip([inp.q, inp.cu_seqlens_q, inp.seq_lens_k, tb], offs, sizes):
             st[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
         stages.append(st)
-    copy_stream = torch.cuda.Stream(dev)
-    cs, ks = ctypes.c_void_p(copy_stream.cuda_stream), ctypes.c_void_p(stream.cuda_stream)
+    in_stream, out_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ins, outs = ctypes.c_void_p(in_stream.cuda_stream), ctypes.c_void_p(out_stream.cuda_stream)
+    ks = ctypes.c_void_p(stream.cuda_stream)
     bufs = []
     for _ in range(2):
         dstage = torch.empty(total, dtype=torch.uint8, device=dev)
@@ -399,16 +402,18 @@ def e2e_pipelined(inp, call, dev, stream, reps, steps):
 
     def step(i):
         b = bufs[i & 1]
-        rt.copy(b["pd"], host_ptrs[i % len(stages)], total, 1, cs)    # host -> device
-        rt.record(b["ev_in"], cs)
+        if i >= 2:
+            rt.wait(ins, b["ev_k"])   # the kernel of step i-2 has read this buffer's inputs
+        rt.copy(b["pd"], host_ptrs[i % len(stages)], total, 1, ins)   # host -> device
+        rt.record(b["ev_in"], ins)
         rt.wait(ks, b["ev_in"])
         if i >= 2:
             rt.wait(ks, b["ev_out"])  # the copy-out of step i-2 has read this buffer's out
         b["prep"]()
         rt.record(b["ev_k"], ks)
-        rt.wait(cs, b["ev_k"])
-        rt.copy(b["ph"], b["po"], out_bytes, 2, cs)                    # device -> host
-        rt.record(b["ev_out"], cs)
+        rt.wait(outs, b["ev_k"])
+        rt.copy(b["ph"], b["po"], out_bytes, 2, outs)                  # device -> host
+        rt.record(b["ev_out"], outs)
 
     for i in range(4):  # warm-up
         step(i)
@@ -554,9 +559,9 @@ def run_ours(args):
                 "note": "public Python API per step (the prepared call of "
                         "varlen_gqa_attention_paged_gb300.prepare): one pinned H2D of q + "
                         "cu_seqlens_q + seq_lens_k + block table (staged together), the call, "
-                        "D2H of out; copies on a copy stream overlap the previous step's "
-                        "kernel (two buffers, events); host wall clock between synchronised "
-                        "ends; the KV cache stays resident"},
+                        "D2H of out; input and output copies on two copy streams overlap "
+                        "the neighbouring steps' kernels (two buffers, events); host wall "
+                        "clock between synchronised ends; the KV cache stays resident"},
         "gpu_launches": call.launches_per_call * args.steps,
         "clocks": clocks,
         "workloads": extra,

@@ -727,23 +727,25 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W, HP>::kThreads,
   if (s_abort && !cmerge) return;
   const bool ok = s_abort == 0;
 
-  // ---- the four warps' states of the same rows: rescale to the rows' max (exchanged
-  // through shared memory), warp 0 adds the others' partial outputs (read in the MMA
-  // fragment layout) and leaves the CTA's partial rows in shared memory.
-  float* const sm_m = reinterpret_cast<float*>(pipe);                  // [W][8]
-  float* const sm_l = sm_m + C::kConsumerWarps * NR;                   // [W][8]
-  float4* const sm_o = reinterpret_cast<float4*>(sm_l + C::kConsumerWarps * NR);  // [W][kMT][32]
+  // ---- the warps' states of the same rows: rescale to the rows' max (exchanged through
+  // shared memory), then every warp leaves its O^T fragments there and warp w adds up
+  // m-tiles w, w + W, ... of all warps (read in the MMA fragment layout) into the CTA's
+  // partial rows.
+  constexpr int W4 = C::kConsumerWarps;
+  float* const sm_m = reinterpret_cast<float*>(pipe);                   // [W][8]
+  float* const sm_l = sm_m + W4 * NR;                                   // [W][8]
+  float4* const sm_o = reinterpret_cast<float4*>(sm_l + W4 * NR);       // [W][kMT][32]
   float* const partial = reinterpret_cast<float*>(pipe + C::kMergeBytes);  // [8][D], m[8], l[8]
   if (gq == 0) {
     sm_m[warp * NR + 2 * cq] = m_run[0];
     sm_m[warp * NR + 2 * cq + 1] = m_run[1];
   }
-  named_bar_sync(1, 32 * C::kConsumerWarps);
+  named_bar_sync(1, 32 * W4);
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * NR + 2 * cq + e]);
+    for (int w = 0; w < W4; ++w) M = fmaxf(M, sm_m[w * NR + 2 * cq + e]);
     const float wt = M == -INFINITY ? 0.f : fast_exp2(m_run[e] - M);
     m_run[e] = M;
     l_run[e] *= wt;
@@ -753,46 +755,42 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W, HP>::kThreads,
       ot[m][e + 2] *= wt;
     }
   }
-  if (warp != 0) {
-    if (gq == 0) {
-      sm_l[warp * NR + 2 * cq] = l_run[0];
-      sm_l[warp * NR + 2 * cq + 1] = l_run[1];
-    }
-#pragma unroll
-    for (int m = 0; m < C::kMT; ++m)
-      sm_o[(warp * C::kMT + m) * 32 + lane] = make_float4(ot[m][0], ot[m][1], ot[m][2], ot[m][3]);
+  if (gq == 0) {
+    sm_l[warp * NR + 2 * cq] = l_run[0];
+    sm_l[warp * NR + 2 * cq + 1] = l_run[1];
   }
-  named_bar_sync(1, 32 * C::kConsumerWarps);
-  if (warp == 0) {
 #pragma unroll
-    for (int w = 1; w < C::kConsumerWarps; ++w) {
-      l_run[0] += sm_l[w * NR + 2 * cq];
-      l_run[1] += sm_l[w * NR + 2 * cq + 1];
+  for (int m = 0; m < C::kMT; ++m)
+    sm_o[(warp * C::kMT + m) * 32 + lane] = make_float4(ot[m][0], ot[m][1], ot[m][2], ot[m][3]);
+  named_bar_sync(1, 32 * W4);
+  // partial rows (v_scale applied): O^T element (m-tile m, fragment row gq + 8h, column
+  // 2cq + e) is output column out_col(m, gq + 8h) of row 2cq + e
+  for (int m = warp; m < C::kMT; m += W4) {
+    float4 o4 = sm_o[m * 32 + lane];
 #pragma unroll
-      for (int m = 0; m < C::kMT; ++m) {
-        const float4 o4 = sm_o[(w * C::kMT + m) * 32 + lane];
-        ot[m][0] += o4.x;
-        ot[m][1] += o4.y;
-        ot[m][2] += o4.z;
-        ot[m][3] += o4.w;
-      }
+    for (int w = 1; w < W4; ++w) {
+      const float4 x = sm_o[(w * C::kMT + m) * 32 + lane];
+      o4.x += x.x;
+      o4.y += x.y;
+      o4.z += x.z;
+      o4.w += x.w;
     }
-    // partial rows (v_scale applied): O^T element (m-tile m, fragment row gq + 8h, column
-    // 2cq + e) is output column out_col(m, gq + 8h) of row 2cq + e
+    const float o[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
-    for (int m = 0; m < C::kMT; ++m)
+    for (int e4 = 0; e4 < 4; ++e4)
+      partial[(2 * cq + (e4 & 1)) * D + C::out_col(m, gq + 8 * (e4 >> 1))] = o[e4] * v_scale;
+  }
+  if (warp == 0 && gq == 0) {
 #pragma unroll
-      for (int e4 = 0; e4 < 4; ++e4)
-        partial[(2 * cq + (e4 & 1)) * D + C::out_col(m, gq + 8 * (e4 >> 1))] = ot[m][e4] * v_scale;
-    if (gq == 0) {
+    for (int e = 0; e < 2; ++e) {
+      float L = 0.f;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        partial[NR * D + 2 * cq + e] = m_run[e];
-        partial[NR * D + NR + 2 * cq + e] = l_run[e];
-      }
+      for (int w = 0; w < W4; ++w) L += sm_l[w * NR + 2 * cq + e];
+      partial[NR * D + 2 * cq + e] = m_run[e];
+      partial[NR * D + NR + 2 * cq + e] = L;
     }
   }
-  named_bar_sync(1, 32 * C::kConsumerWarps);
+  named_bar_sync(1, 32 * W4);
 
   const size_t n_part = static_cast<size_t>(p.n_part);
   const size_t esz = p.out_dtype == UA_DT_F32 ? 4 : 2;

@@ -186,21 +186,21 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// LSE merge of one output row over the np (<= 16) split partitions of a thread-block
-// cluster, by one warp (the merge of the split path):
+// LSE merge of one output row over the np (1 <= np <= 16) split partitions of a
+// thread-block cluster, by one warp (the merge of the split path):
 //   M = max_{l_z > 0} m_z,  L = sum l_z 2^(m_z - M),  out = sum acc_z 2^(m_z - M) / L.
 // Partition zz is the cluster's CTA rank0 + rank_step * zz; in its shared memory the row's
 // max and sum sit at byte offsets m_off and l_off and its partial row (D floats) at
 // row_off.  Every partition's max, sum and slice of the row are loaded before any is used
-// (at most 64 floats a lane in flight), so the round trips through distributed shared
-// memory overlap.  An empty partition weighs 0 (its partial row is 0).  Writes the
-// normalised row to dst in out_dtype.
+// (warp-uniform branches, no selects on loaded values), so the round trips through
+// distributed shared memory overlap.  An empty partition weighs 0 (its partial row is 0).
+// Writes the normalised row to dst in out_dtype.
 template <int D>
 __device__ __forceinline__ void cluster_merge_row(uint32_t m_off, uint32_t l_off,
                                                   uint32_t row_off, int np, uint32_t rank0,
                                                   uint32_t rank_step, int lane, uint8_t* dst,
                                                   int out_dtype) {
-  constexpr int kPer = D / 32;                     // columns a lane merges
+  constexpr int kPer = D / 32;                       // columns a lane merges
   constexpr int kBatch = kPer > 4 ? 64 / kPer : 16;  // partitions loaded at once
   float mz = -INFINITY, lz = 0.f;
   if (lane < np) {
@@ -212,10 +212,9 @@ __device__ __forceinline__ void cluster_merge_row(uint32_t m_off, uint32_t l_off
   auto load = [&](int z0) {
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) v[i][e] = 0.f;
-      if (z0 + i < np) {
-        const uint32_t a = cluster_map(row_off + lane * kPer * 4, rank0 + rank_step * (z0 + i));
+      if (z0 + i < np) {  // uniform
+        const uint32_t a =
+            cluster_map(row_off + lane * kPer * 4, rank0 + rank_step * (z0 + i));
         if constexpr (kPer >= 4) {
 #pragma unroll
           for (int e = 0; e < kPer; e += 4) {
@@ -250,7 +249,7 @@ __device__ __forceinline__ void cluster_merge_row(uint32_t m_off, uint32_t l_off
       if (z0 + i < np) {  // uniform
         const float wt = __shfl_sync(0xffffffffu, wz, z0 + i);
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] += v[i][e] * wt;
+        for (int e = 0; e < kPer; ++e) acc[e] = fmaf(v[i][e], wt, acc[e]);
       }
     }
   }
