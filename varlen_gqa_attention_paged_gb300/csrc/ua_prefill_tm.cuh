@@ -50,8 +50,8 @@
 
 namespace ua {
 
-// SW: softmax warps per tensor-memory lane quarter of a q tile (1, or 2 splitting the key
-// columns of S and the columns of O between them).
+// SW: softmax warps per tensor-memory lane quarter of a q tile (1, or 2 or 4 splitting the
+// key columns of S and the columns of O between them).
 template <int D, int NQ, bool F8 = false, int SW = 1>
 struct PrefillTmCfg {
   static constexpr int kBM = 128;                        // MMA rows of one q tile
@@ -78,7 +78,8 @@ struct PrefillTmCfg {
   static constexpr int kTmemStride = kBN + D;            // S/P, then O, of one q tile
   static constexpr int kTmemCols = 512;
   static constexpr int kSoftmaxWarps = 4 * NQ * SW;
-  static_assert(SW == 1 || SW == 2, "one or two softmax warps per lane quarter");
+  static_assert(SW == 1 || SW == 2 || (SW == 4 && D == 128),
+                "one, two or (head_dim 128) four softmax warps per lane quarter");
   static constexpr int kThreads = 32 * kSoftmaxWarps + 96 + 32 * kDeqWarps;
   static_assert(D <= 128, "two 128-key K/V rings must fit");
   static_assert(NQ * kTmemStride <= kTmemCols, "tensor memory budget");
@@ -189,6 +190,11 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   if (warp == kMma) {
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
+  }
+  if (warp == kProducerK && lane == 0) {
+    tma_prefetch_desc(&pp.tmap_q);
+    tma_prefetch_desc(&pp.tmap_k);
+    tma_prefetch_desc(&pp.tmap_v);
   }
   tc_fence_before();
   __syncthreads();
@@ -638,11 +644,12 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       // or a mask get it here, once, and are written back over S for pass 2.
       const bool rewrite = FEAT || need_mask;
       float mx0 = -INFINITY, mx1 = -INFINITY;
+      constexpr bool kTwo = kCols >= 64;  // two 32-column loads an iteration
 #pragma unroll 1
-      for (int c0 = half * kCols; c0 < (half + 1) * kCols; c0 += 64) {
+      for (int c0 = half * kCols; c0 < (half + 1) * kCols; c0 += kTwo ? 64 : 32) {
         uint32_t ra[32], rb[32];
         tmem_ld32(tS + c0, ra);
-        tmem_ld32(tS + c0 + 32, rb);
+        if constexpr (kTwo) tmem_ld32(tS + c0 + 32, rb);
         tmem_ld_wait();
         if (rewrite) {
           const float ab = FEAT ? slope * static_cast<float>(k0 + c0 - ctx) : 0.f;
@@ -650,22 +657,24 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, ab, e, std::true_type{}));
-              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::true_type{}));
+              if constexpr (kTwo)
+                rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::true_type{}));
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               ra[e] = __float_as_uint(score(__uint_as_float(ra[e]), k0 + c0 + e, ab, e, std::false_type{}));
-              rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::false_type{}));
+              if constexpr (kTwo)
+                rb[e] = __float_as_uint(score(__uint_as_float(rb[e]), k0 + c0 + 32 + e, ab, 32 + e, std::false_type{}));
             }
           }
           tmem_st32(tS + c0, ra);
-          tmem_st32(tS + c0 + 32, rb);
+          if constexpr (kTwo) tmem_st32(tS + c0 + 32, rb);
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           mx0 = fmax3(mx0, __uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(rb[e]), __uint_as_float(rb[e + 1]));
+          if constexpr (kTwo) mx1 = fmax3(mx1, __uint_as_float(rb[e]), __uint_as_float(rb[e + 1]));
         }
       }
       if (rewrite) tmem_st_wait();
@@ -779,16 +788,33 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
         mbar_arrive(&xbar[1]);
         ok = pf_wait_warp(&xbar[1], 0, abort_flag, p.status);
         tc_fence_after();
-        uint32_t l0, l1;
-        tmem_ld2(tS0, l0, l1);
-        tmem_ld_wait();
-        l = __uint_as_float(l0) + __uint_as_float(l1);
+        if constexpr (SW == 2) {
+          uint32_t l0, l1;
+          tmem_ld2(tS0, l0, l1);
+          tmem_ld_wait();
+          l = __uint_as_float(l0) + __uint_as_float(l1);
+        } else {
+          uint32_t l4[4];
+          tmem_ld4(tS0, l4);
+          tmem_ld_wait();
+          l = (__uint_as_float(l4[0]) + __uint_as_float(l4[1])) +
+              (__uint_as_float(l4[2]) + __uint_as_float(l4[3]));
+        }
       }
     }
-    if (ok) {
+    if (ok && active) {
       const size_t orow = static_cast<size_t>(q0 + i_q) * p.hq + h;
       const size_t n_part = static_cast<size_t>(p.n_part);
       const float inv = l > 0.f ? v_mul / l : 0.f;
+      // One q tile: a split's partial rows leave through a 4 KB slice of the K/V ring that
+      // this warp alone owns now (the ring's last reader, the tile's last P.V, is complete),
+      // so that each store writes whole 128-byte runs of four rows instead of 16 bytes of 32
+      // rows; only for warps with more than a quarter of their rows valid (a decode row or
+      // two store faster straight from their lanes).  (In the two-tile kernel the same code
+      // measured 5 % slower on the fp8 long prefill, which never splits: left out there.)
+      const long long wrow = rv ? static_cast<long long>(orow * n_part + z) : -1;
+      const bool staged = NQ == 1 && n_part > 1 && n_tiles > 0 &&
+                          __popc(__ballot_sync(0xffffffffu, rv)) > 8;
 #pragma unroll 1
       for (int c0 = half * kOCols; c0 < (half + 1) * kOCols; c0 += 32) {
         uint32_t rr[32];
@@ -799,8 +825,53 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = 0u;
         }
+        if constexpr (NQ == 1) {
+          if (staged) {
+            // this lane's row, 16-byte chunk k at position k ^ (row mod 8) (conflict-free
+            // both ways); then lane l copies chunk l mod 8 of rows l / 8 + 4 j
+            float* const stg = reinterpret_cast<float*>(sK) + (warp % (4 * SW)) * 1024;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(stg + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+                  make_float4(__uint_as_float(rr[4 * k]) * v_mul,
+                              __uint_as_float(rr[4 * k + 1]) * v_mul,
+                              __uint_as_float(rr[4 * k + 2]) * v_mul,
+                              __uint_as_float(rr[4 * k + 3]) * v_mul);
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int rw = (lane >> 3) + 4 * j, ck = lane & 7;
+              const unsigned hi32 = static_cast<unsigned>(
+                  __shfl_sync(0xffffffffu, static_cast<int>(wrow >> 32), rw));
+              const unsigned lo32 =
+                  static_cast<unsigned>(__shfl_sync(0xffffffffu, static_cast<int>(wrow), rw));
+              const long long wr =
+                  static_cast<long long>((static_cast<unsigned long long>(hi32) << 32) | lo32);
+              const float4 v =
+                  *reinterpret_cast<const float4*>(stg + rw * 32 + ((ck ^ (rw & 7)) << 2));
+              if (wr >= 0) *reinterpret_cast<float4*>(p.ws_acc + wr * D + c0 + 4 * ck) = v;
+            }
+            __syncwarp();
+            if (rv && c0 == 0) {
+              p.ws_m[wrow] = m_used;
+              p.ws_l[wrow] = l;
+            }
+            continue;
+          }
+        }
         if (!rv) continue;
-        if (n_part == 1) {
+        if (n_part > 1) {  // the partition's max, sum and unnormalised row
+          const size_t w = orow * n_part + z;
+          if (c0 == 0) {
+            p.ws_m[w] = m_used;
+            p.ws_l[w] = l;
+          }
+          float4* dst = reinterpret_cast<float4*>(p.ws_acc + w * D + c0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(rr[4 * e]) * v_mul, __uint_as_float(rr[4 * e + 1]) * v_mul,
+                                 __uint_as_float(rr[4 * e + 2]) * v_mul, __uint_as_float(rr[4 * e + 3]) * v_mul);
+        } else {
           if (p.out_dtype == UA_DT_F32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + c0);
 #pragma unroll
@@ -821,17 +892,6 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
               dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
-        } else {
-          const size_t w = orow * n_part + z;
-          if (c0 == 0) {
-            p.ws_m[w] = m_used;
-            p.ws_l[w] = l;
-          }
-          float4* dst = reinterpret_cast<float4*>(p.ws_acc + w * D + c0);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(rr[4 * e]) * v_mul, __uint_as_float(rr[4 * e + 1]) * v_mul,
-                                 __uint_as_float(rr[4 * e + 2]) * v_mul, __uint_as_float(rr[4 * e + 3]) * v_mul);
         }
       }
     }
@@ -842,13 +902,15 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
   if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// One q tile a CTA: two softmax warps per lane quarter (a CTA would otherwise have one
-// softmax warp per SM sub-partition).  Two q tiles already alternate on the tensor cores;
-// splitting their softmax too measured slower on GB300 (the d128 long prefill went from
-// 1.12 to 1.19 ms).
+// One q tile a CTA: four softmax warps per lane quarter at head_dim 128 with a 16-bit cache
+// (32 key columns a warp: the per-tile chain of a thread shortens; the mixed batch went
+// from 24.5 to 22 us against two), two at head_dim 64 (O's 64 columns) and for fp8 caches
+// (the dequant warps' registers).  A CTA would otherwise have one softmax warp per SM
+// sub-partition.  Two q tiles already alternate on the tensor cores; splitting their
+// softmax too measured slower on GB300 (the d128 long prefill went from 1.12 to 1.19 ms).
 template <int D, int NQ, bool BF16, bool FEAT, bool F8 = false>
 cudaError_t launch_prefill_tm_t(const PrefillParams& pp, dim3 grid, cudaStream_t stream) {
-  constexpr int SW = NQ == 1 ? 2 : 1;
+  constexpr int SW = NQ == 1 ? (D == 128 && !F8 ? 4 : 2) : 1;
   using C = PrefillTmCfg<D, NQ, F8, SW>;
   auto kern = ua_prefill_tm_kernel<D, NQ, BF16, FEAT, F8, SW>;
   static std::atomic<unsigned long long> configured{0};  // one bit per device

@@ -94,8 +94,6 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
   constexpr int kDeq0 = kMma + 1;  // fp8: dequant warps kDeq0 .. kDeq0 + 3
   static_assert(!F8 || !BF16, "fp8 caches run the f16 MMAs");
   const AttnParams& p = pp.p;
-  grid_dependency_wait();
-  grid_launch_dependents();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* const smem = reinterpret_cast<uint8_t*>(
@@ -127,23 +125,6 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
   const int z = blockIdx.z;
   const int G = p.group;
   const int TQ = pp.tq;
-
-  // Longest walks first: slots are taken in reverse order.
-  const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
-  const PfSeq sq = pf_seq_of_slot(p.cu_seqlens_q, p.seq_lens_k, p.num_seqs, x, TQ);
-  const int b = sq.b, q0 = sq.q0, q_len = sq.q_len, kv_len = sq.kv_len;
-  const int t_first = (x - (q0 / TQ + b)) * TQ;
-  if (t_first < 0 || t_first >= q_len) return;   // idle slot: uniform for the CTA
-  const int t_last = min(t_first + TQ, q_len) - 1;
-  const int ctx = kv_len - q_len;
-  const int pos_first = ctx + t_first, pos_last = ctx + t_last;
-  const int hi = max(0, min(pos_last + 1, kv_len));
-  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
-  int part = (hi - lo + p.n_part - 1) / p.n_part;
-  part = (part + 15) & ~15;
-  const int ks = min(lo + z * part, hi);
-  const int ke = min(ks + part, hi);
-  const int nt = (ke - ks + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -183,12 +164,41 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&pp.tmap_q);
+    tma_prefetch_desc(&pp.tmap_k);
+    tma_prefetch_desc(&pp.tmap_v);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tO = tmem + 2 * BN;
   volatile int* abort_flag = &s_abort;
+  // Everything above touches only this CTA's shared and tensor memory, so it overlaps the
+  // previous kernel's tail (programmatic dependent launch); global memory is read below.
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  // Longest walks first: slots are taken in reverse order.
+  const int x = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  const PfSeq sq = pf_seq_of_slot(p.cu_seqlens_q, p.seq_lens_k, p.num_seqs, x, TQ);
+  const int b = sq.b, q0 = sq.q0, q_len = sq.q_len, kv_len = sq.kv_len;
+  const int t_first = (x - (q0 / TQ + b)) * TQ;
+  if (t_first < 0 || t_first >= q_len) {  // idle slot: uniform for the CTA
+    if (warp == kMma) tmem_dealloc(tmem, C::kTmemCols);
+    return;
+  }
+  const int t_last = min(t_first + TQ, q_len) - 1;
+  const int ctx = kv_len - q_len;
+  const int pos_first = ctx + t_first, pos_last = ctx + t_last;
+  const int hi = max(0, min(pos_last + 1, kv_len));
+  const int lo = min(hi, p.window_left >= 0 ? max(0, pos_first - p.window_left) : 0) & ~15;
+  int part = (hi - lo + p.n_part - 1) / p.n_part;
+  part = (part + 15) & ~15;
+  const int ks = min(lo + z * part, hi);
+  const int ke = min(ks + part, hi);
+  const int nt = (ke - ks + BN - 1) / BN;
 
   if (warp >= 4 && warp < 4 + C::kProducers) {
     // ======================================================== TMA producers
