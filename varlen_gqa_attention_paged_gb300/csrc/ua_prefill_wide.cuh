@@ -44,8 +44,8 @@
 namespace ua {
 
 // F8: fp8-e4m3 caches.  The producers copy each half tile of codes (128 keys x 128 bytes)
-// into a two-slot staging ring, and four dequant warps (thread = key) write it into its f16
-// slot, exactly (every e4m3 value is an f16), so the f16 MMAs and the softmax run
+// into a two-slot staging ring, and eight dequant warps (thread = one key's 64-column half)
+// write it into its f16 slot, exactly (every e4m3 value is an f16), so the f16 MMAs and the softmax run
 // unchanged; k_scale joins the score scale and v_scale the output (per-token scales:
 // folded into each key's f16 row instead).
 template <int D, bool F8 = false>
@@ -69,7 +69,9 @@ struct PrefillWideCfg {
   // items as there are producers (a producer's parity wait is then never more than one
   // phase behind).
   static constexpr int kProducers = F8 ? 2 : 4;
-  static constexpr int kDeqWarps = F8 ? 4 : 0;
+  // eight dequant warps: thread = (key, column half); with four (thread = key) each item's
+  // conversion took twice as long on the critical path
+  static constexpr int kDeqWarps = F8 ? 8 : 0;
   static constexpr int kThreads = 32 * (4 + kProducers + 1 + kDeqWarps);
   static_assert(D == 256, "two half tiles of 128 columns");
   static_assert(2 * kBN + D <= kTmemCols, "tensor memory budget");
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
   constexpr int BN = C::kBN;
   constexpr int NS = C::kSlots;
   constexpr int kMma = 4 + C::kProducers;
-  constexpr int kDeq0 = kMma + 1;  // fp8: dequant warps kDeq0 .. kDeq0 + 3
+  constexpr int kDeq0 = kMma + 1;  // fp8: dequant warps kDeq0 .. kDeq0 + 7
   static_assert(!F8 || !BF16, "fp8 caches run the f16 MMAs");
   const AttnParams& p = pp.p;
 
@@ -367,17 +369,19 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
     umma_commit_warp(fin);
     mbar_wait_bounded(fin, 0, p.status, DEV_TIMEOUT);
   } else if (F8 && warp >= kDeq0) {
-    // ======================================================== fp8 dequant warps (thread = key)
-    // Q (bf16) to f16 in place once; then every item of the slot sequence: the staged half
-    // tile of codes (128-byte rows, 128-byte swizzled) into its f16 slot (two 128-byte
-    // swizzled column blocks), each e4m3 value exactly, or times the key's own scale
-    // (per-token scales); V rows of keys at or past kv_len become zeros.
-    const int td = (warp - kDeq0) * 32 + lane;
+    // ======================================================== fp8 dequant warps
+    // Thread (key td, column half hc): Q (bf16) to f16 in place once (row td, column blocks
+    // of half hc); then every item of the slot sequence: codes 64 hc .. 64 hc + 63 of the
+    // staged half tile (128-byte rows, 128-byte swizzled) into column block hc of its f16
+    // slot, each e4m3 value exactly, or times the key's own scale (per-token scales); V
+    // rows of keys at or past kv_len become zeros.
+    const int tdh = (warp - kDeq0) * 32 + lane;
+    const int td = tdh & (BN - 1), hc = tdh / BN;
     const uint32_t sw = td & 7;
     bool ok = pf_wait_warp(q_full, 0, abort_flag, p.status);
     if (ok && p.q_dtype == UA_DT_BF16) {
 #pragma unroll 1
-      for (int cb = 0; cb < C::kCB; ++cb) {
+      for (int cb = hc * (C::kCB / 2); cb < (hc + 1) * (C::kCB / 2); ++cb) {
         uint4* row = reinterpret_cast<uint4*>(sQ + cb * C::kBM * 128 + td * 128);
 #pragma unroll
         for (int c0 = 0; c0 < 8; ++c0) {  // element-wise: the order only spreads the banks
@@ -425,12 +429,13 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
       const float ts = tok ? key_scale(j, is_k) : 1.f;
       const int st = u % C::kStage;
       if (!pf_wait_warp(&s8_full[st], (u / C::kStage) & 1, abort_flag, p.status)) { ok = false; break; }
-      // take the row of codes into registers and hand the staging slot back at once
-      uint4 raw[8];
+      // take the half row of codes into registers and hand the staging slot back at once
+      uint4 raw[4];
       {
         const uint8_t* src = s8 + st * C::kStageBytes + td * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+        for (int c = 0; c < 4; ++c)
+          raw[c] = *reinterpret_cast<const uint4*>(src + (((4 * hc + c) ^ sw) << 4));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s8_empty[st]);
@@ -442,8 +447,9 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
       uint8_t* dst = sR + sl * C::kSlotBytes + td * 128;
       const bool zero = !is_k && ks + j * BN + td >= kv_len;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 16 codes of the row -> f16 chunks 2c, 2c + 1
-        const uint4 r = zero ? make_uint4(0, 0, 0, 0) : raw[c];
+      for (int c4 = 0; c4 < 4; ++c4) {  // 16 codes of the row -> f16 chunks 2c, 2c + 1
+        const int c = 4 * hc + c4;
+        const uint4 r = zero ? make_uint4(0, 0, 0, 0) : raw[c4];
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
         uint32_t hh[8];
 #pragma unroll
