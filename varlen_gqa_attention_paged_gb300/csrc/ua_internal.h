@@ -56,18 +56,16 @@ struct TileParams {
   AttnParams p;
 };
 
-// Tensor-memory prefill kernel launch argument: tensor maps of q (viewed as [H_q][total_q][D],
-// box 64 elements x tq tokens x G heads, so a tile's rows are head-major; or, if that view
-// cannot be encoded, [total_q][H_q][D] with token-major rows) and of the two caches, the
-// attention parameters, and tq = query tokens per 128-row q tile (floor(128 / G)); a CTA
-// owns 1 or 2 such tiles of consecutive tokens.
+// Tensor-memory prefill kernel launch argument: tensor maps of q (viewed as [total_q][H_q][D],
+// box 64 elements x G heads x tq tokens, so a tile's row token * G + head) and of the two
+// caches, the attention parameters, and tq = query tokens per 128-row q tile
+// (floor(128 / G)); a CTA owns 1 or 2 such tiles of consecutive tokens.
 struct PrefillParams {
   CUtensorMap tmap_q;
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
   AttnParams p;
   int tq;
-  int q_head_major;  // 1: tile row = head * tq + token (tmap_q boxes {64, tq, G}); 0: token * G + head
 };
 
 // The LSE-merge of split partitions (one output row per query token x head).

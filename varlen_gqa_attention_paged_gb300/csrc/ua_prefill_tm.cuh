@@ -262,9 +262,8 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
       mbar_arrive_expect_tx(q_full, nq_act * C::kCB * TQ * G * 128);
       for (int qt = 0; qt < nq_act; ++qt)
         for (int cb = 0; cb < C::kCB; ++cb)
-          tma_load_3d_pf(sQ + qt * C::kQBytes + cb * C::kBM * 128, &pp.tmap_q, 64 * cb,
-                         pp.q_head_major ? q0 + t_first + qt * TQ : g * G,
-                         pp.q_head_major ? g * G : q0 + t_first + qt * TQ, q_full);
+          tma_load_3d_pf(sQ + qt * C::kQBytes + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G,
+                         q0 + t_first + qt * TQ, q_full);
     }
     // block id of this lane's 16-key page of key tile j (lanes 0 .. BN/16-1; -1: none)
     auto page_blk = [&](int j) -> int {
@@ -562,14 +561,14 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     tile_walk(qt, jb, je);
     const int n_tiles = je - jb;
     const int tf = t_first + qt * TQ;
-    // the row's token within the tile and head within the group (head-major or token-major rows)
-    const int tl = pp.q_head_major ? r % TQ : r / G;
+    // the row's token within the tile and head within the group (rows token * G + head)
+    const int tl = r / G;
     const bool rv = qt < nq_act && r < TQ * G && tf + tl < q_len && q0 + tf + tl < p.total_q;
     // a warp none of whose rows holds a query row (a q tile's unused rows) only keeps the
     // tile barriers in step: what its rows of P and O hold is never stored
     const bool active = __any_sync(0xffffffffu, rv);
     const int i_q = tf + (rv ? tl : 0);                    // query index within the sequence
-    const int h = g * G + (pp.q_head_major ? r / TQ : r % G);
+    const int h = g * G + r % G;
     const int pos = ctx + i_q;
     const int lo_r = p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
     // warp-uniform bounds of this warp's valid rows, to mask only boundary tiles

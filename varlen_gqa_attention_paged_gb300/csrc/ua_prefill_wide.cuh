@@ -219,9 +219,7 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
     if (pw == 0 && lane == 0) {
       mbar_arrive_expect_tx(q_full, C::kCB * TQ * G * 128);
       for (int cb = 0; cb < C::kCB; ++cb)
-        tma_load_3d_pf(sQ + cb * C::kBM * 128, &pp.tmap_q, 64 * cb,
-                       pp.q_head_major ? q0 + t_first : g * G, pp.q_head_major ? g * G : q0 + t_first,
-                       q_full);
+        tma_load_3d_pf(sQ + cb * C::kBM * 128, &pp.tmap_q, 64 * cb, g * G, q0 + t_first, q_full);
     }
     const int n_items = 4 * nt;
     // item u: K or V, tile j, half h
@@ -475,11 +473,11 @@ __global__ void __launch_bounds__(PrefillWideCfg<D, F8>::kThreads, 1)
   } else {
     // ======================================================== softmax warps (thread = row)
     const int r = 32 * warp + lane;
-    // the row's token within the tile and head within the group (head-major or token-major rows)
-    const int tl = pp.q_head_major ? r % TQ : r / G;
+    // the row's token within the tile and head within the group (rows token * G + head)
+    const int tl = r / G;
     const bool rv = r < TQ * G && tl <= t_last - t_first && q0 + t_first + tl < p.total_q;
     const int i_q = t_first + (rv ? tl : 0);
-    const int h = g * G + (pp.q_head_major ? r / TQ : r % G);
+    const int h = g * G + r % G;
     const int pos = ctx + i_q;
     const int lo_r = p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
     int pmin = rv ? pos : INT_MAX, lomax = rv ? lo_r : INT_MIN;
