@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(PrefillTmCfg<D, NQ, F8, SW>::kThreads, 1)
     // [half D / SW, (half + 1) D / SW).  Once per tile their row maxima meet in shared
     // memory, each rounded up to bf16, and every warp of the row takes the largest: the
     // same running max in every warp, never below the true one.  Their row sums meet at
-    // the end through two columns of the tile's S/P region, free after its last P.V.
+    // the end through SW columns of the tile's S/P region, free after its last P.V.
     constexpr int kCols = BN / SW, kOCols = D / SW;
     const int qt = warp / (4 * SW);                        // q tile of this warp
     const int quad = warp & 3;                             // its tensor-memory lane quarter
