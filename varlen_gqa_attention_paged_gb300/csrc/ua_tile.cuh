@@ -181,7 +181,14 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
                : "memory");
 }
 
-// The mbarrier receives one arrival once this thread's earlier cp.async copies land.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
+// The mbarrier's pending count rises by one now and falls once this thread's earlier
+// cp.async copies land (no net arrival).
+
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
