@@ -24,6 +24,12 @@
 
 namespace ua {
 
+// Bring the line holding `ptr` into L2 (a hint: no value is read, and L2 is coherent, so a
+// write by an earlier kernel is never missed by a later load).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // W consumer warps (4, or 8 for grids of at most one CTA per SM), each taking 16 keys of
 // every stage.  HP kv-heads per CTA (1, or 2 for fp8 caches with at most 4 rows per kv-head:
 // the two heads' q-blocks share the MMA's 8 columns, and one page box carries both heads).
@@ -137,9 +143,16 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W, HP>::kThreads,
     s_abort = 0;
     mbar_fence_init();
   }
-  if (warp == C::kConsumerWarps && lane == 0) {
-    tma_prefetch_desc(&tp.tmap_k);
-    tma_prefetch_desc(&tp.tmap_v);
+  if (warp == C::kConsumerWarps) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tp.tmap_k);
+      tma_prefetch_desc(&tp.tmap_v);
+      prefetch_l2(p.cu_seqlens_q + blockIdx.x);
+      prefetch_l2(p.seq_lens_k + blockIdx.x);
+    }
+    // the sequence's block-table row (slot x is sequence x), one 128-byte line a lane
+    const int32_t* btr = p.block_table + static_cast<size_t>(blockIdx.x) * p.max_blocks_per_seq;
+    for (int i = 32 * lane; i < p.max_blocks_per_seq; i += 32 * 32) prefetch_l2(btr + i);
   }
   __syncthreads();
   grid_dependency_wait();
