@@ -150,9 +150,11 @@ __global__ void __launch_bounds__(DecCfg<D, KV, W, HP>::kThreads,
       prefetch_l2(p.cu_seqlens_q + blockIdx.x);
       prefetch_l2(p.seq_lens_k + blockIdx.x);
     }
-    // the sequence's block-table row (slot x is sequence x), one 128-byte line a lane
+    // the sequence's block-table row (slot x is sequence x), one 128-byte line a lane, up to
+    // 256 lines (8192 pages)
     const int32_t* btr = p.block_table + static_cast<size_t>(blockIdx.x) * p.max_blocks_per_seq;
-    for (int i = 32 * lane; i < p.max_blocks_per_seq; i += 32 * 32) prefetch_l2(btr + i);
+    const int bt_end = min(p.max_blocks_per_seq, 256 * 32);
+    for (int i = 32 * lane; i < bt_end; i += 32 * 32) prefetch_l2(btr + i);
   }
   __syncthreads();
   grid_dependency_wait();
