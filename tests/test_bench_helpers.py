@@ -9,7 +9,9 @@ import workloads as W
 
 
 def test_kernel_name_follows_the_plan():
-    assert bench.kernel_name({"kernel": 2}, 128) == "ua_decode_kernel"
+    # the key-major decode tile: four consumer warps (2), eight (32), two kv-heads a CTA (64)
+    for k in (2, 32, 64):
+        assert bench.kernel_name({"kernel": k}, 128) == "ua_decode_kernel"
     assert bench.kernel_name({"kernel": 1}, 256) == "ua_attn_tile_kernel"
     assert bench.kernel_name({"kernel": 4}, 64) == "ua_attn_tile_kernel"
     for k in (8, 16):
